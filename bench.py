@@ -1,0 +1,406 @@
+#!/usr/bin/env python
+"""Benchmark of the fused top-K KL distillation loss, forward + backward.
+
+One step = kd_topk_kl_forward + kd_topk_kl_backward over one synthetic batch
+(every step of the loss: teacher prep, logit GEMM with online lse + gather,
+combine, and per row chunk the logit recompute with the gradient epilogue, dh
+and dW contractions).  Default workload: ctx_32k (T=32768, V=201088, d=2880,
+K=100, tau=1, 10% rows masked), inputs resident in HBM and larger than L2.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun), every rank runs its own
+batch (replicas, weak scaling, no collective on the data path); the timed
+region is bracketed by barriers and the max over ranks is reported.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same
+workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused top-K KL fwd+bwd tokens/s (T=32k,V=201k,d=2880); % bf16 TC peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ---------------------------------------------------------------- ranks
+
+def rank_info():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_setup(world: int, backend: str):
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world: int):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """Max of a per-rank scalar (the slowest rank sets the job time)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job units/s: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / max_seconds
+
+
+# ---------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling (200 ms) while the timed region runs."""
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="kd_clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        return parse_clock_csv(open(self.path).read())
+
+
+def parse_clock_csv(text: str) -> dict:
+    sm, smax, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in text.strip().splitlines():
+        f = [c.strip() for c in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            sm.append(float(f[1]))
+            smax.append(float(f[2]))
+            power.append(float(f[3]))
+        except ValueError:
+            continue
+        for n, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+    return {"sm_mhz": float(statistics.median(sm)), "sm_max_mhz": float(max(smax)),
+            "power_w_max": float(max(power)), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, only if
+    the kernel sources still hash to what was profiled (else None)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunked_top_kl_logit_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != d.get("csrc_sha256"):
+        return None
+    return d.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def blas_threads() -> int:
+    try:
+        import threadpoolctl
+        n = [i.get("num_threads", 0) for i in threadpoolctl.threadpool_info()
+             if i.get("internal_api") in ("openblas", "mkl", "blis")]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def oracle_sample(w, rows: int, seed: int = 0):
+    """A `rows`-row sample of workload `w` (full V, d), as the oracle sees it."""
+    from synth import make_inputs
+    x = make_inputs(w.replace(T=rows), seed=seed)
+    return dict(h=x["h"].to(torch.bfloat16).double().numpy(),
+                W=x["W"].to(torch.bfloat16).double().numpy(),
+                idx=x["teacher_idx"].numpy(), tl=x["teacher_logits"].double().numpy(),
+                valid=x["valid"].numpy(), tau=w.tau)
+
+
+def oracle_step_seconds(s) -> float:
+    """Wall time of the fp64 oracle's forward + backward on sample `s`."""
+    from oracle import kd_oracle as O
+    t0 = time.perf_counter()
+    f = O.forward(s["h"], s["W"], s["idx"], s["tl"], s["valid"], s["tau"])
+    O.backward(s["h"], s["W"], s["idx"], s["tl"], s["valid"], s["tau"], 1.0, lse=f["lse"])
+    return time.perf_counter() - t0
+
+
+def run_reference(args, w, world, rank):
+    if rank != 0:
+        return None
+    rows = args.ref_rows
+    s = oracle_sample(w, rows)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt = oracle_step_seconds(s)
+        if i >= args.warmup:
+            times.append(dt)
+    sec = statistics.mean(times)
+    value = rows / sec
+    sample = (f"fp64 oracle fwd+bwd on a {rows}-row sample of {w.name} "
+              f"(full V={w.V}, d={w.d}) per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(w, args.chunk or w.chunk),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def workload_config(w, chunk):
+    return {"workload": w.name, "T": w.T, "V": w.V, "d": w.d, "K": w.K, "tau": w.tau,
+            "chunk": chunk, "mask": w.mask_kind, "teacher_idx": w.idx_kind,
+            "l2": "inputs larger than L2 (W alone is V*d*2 B)"}
+
+
+# ---------------------------------------------------------------- GPU run
+
+def run_ours(args, w, world, rank, local_rank):
+    import chunked_top_kl_logit_b300 as kd
+    from synth import make_inputs
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    chunk = args.chunk or w.chunk
+    x = make_inputs(w, seed=args.seed + rank, device=dev)
+    T, V, d, K, tau = w.T, w.V, w.d, w.K, w.tau
+    h = x["h"].to(dev)
+    W = x["W"].to(dev)
+    idx = x["teacher_idx"].to(dev)
+    tl = x["teacher_logits"].to(dev)
+    valid = x["valid"].to(dev)
+    n_valid = int(x["valid"].sum())
+
+    torch.cuda.synchronize()
+    base_alloc = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    m = kd.TopKKL(T, V, d, K, chunk, device=dev)
+
+    def step():
+        m.forward(h, W, idx, tl, valid, tau)
+        m.backward(h, W, idx, tl, valid, tau, 1.0)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    kd.check_device_status(m.status, "warm-up step")
+    peak = torch.cuda.max_memory_allocated(dev)
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id).start()
+    time.sleep(0.3)
+    n = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(n):
+        ev[i][0].record()
+        m.forward(h, W, idx, tl, valid, tau)
+        ev[i][1].record()
+        m.backward(h, W, idx, tl, valid, tau, 1.0)
+        ev[i][2].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    kd.check_device_status(m.status, "timed steps")
+    total_ms = ev[0][0].elapsed_time(ev[n - 1][2])
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    bwd_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+    max_sec = max_over_ranks(total_ms / 1e3, world, device=dev)
+    ms_per_step = max_sec * 1e3 / n
+    value = job_throughput(T * n, world, max_sec)
+
+    # end to end through the public API: pinned host inputs -> device, fwd+bwd,
+    # outputs (loss, lse, dh, dW) -> pinned host, every step
+    e2e = None
+    if not args.no_e2e:
+        hin = {k: v.pin_memory() for k, v in (("h", x["h"]), ("W", x["W"]), ("idx", x["teacher_idx"]),
+                                                 ("tl", x["teacher_logits"]), ("valid", x["valid"]))}
+        dinp = {"h": h, "W": W, "idx": idx, "tl": tl, "valid": valid}
+        hout = {"loss": torch.empty(1, pin_memory=True), "lse": torch.empty(T, pin_memory=True),
+                "dh": torch.empty(T, d, pin_memory=True), "dW": torch.empty(V, d, pin_memory=True)}
+        dout = {"loss": m.loss, "lse": m.lse, "dh": m.dh, "dW": m.dW}
+
+        def e2e_step():
+            for k in dinp:
+                dinp[k].copy_(hin[k], non_blocking=True)
+            m.forward(h, W, idx, tl, valid, tau)
+            m.backward(h, W, idx, tl, valid, tau, 1.0)
+            for k in dout:
+                hout[k].copy_(dout[k], non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        ne = max(1, min(n, 5))
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        s0.record()
+        for _ in range(ne):
+            e2e_step()
+        s1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        kd.check_device_status(m.status, "e2e steps")
+        e2e_sec = max_over_ranks(s0.elapsed_time(s1) / 1e3, world, device=dev)
+        e2e = {"value": job_throughput(T * ne, world, e2e_sec), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hin.values())),
+               "d2h_bytes_per_step": int(sum(t.numel() * t.element_size() for t in hout.values())),
+               "ms_per_step": e2e_sec * 1e3 / ne, "steps": ne}
+
+    peaks, peak_src = load_peaks()
+    flops_nominal = 8.0 * T * d * V
+    flops_alg = (2.0 * T + 6.0 * n_valid) * d * V
+    tf_nominal = flops_nominal / (ms_per_step / 1e3) / 1e12 * world
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    fwd_tf = 2.0 * T * d * V / (fwd_ms / 1e3) / 1e12
+    fl, bl = kd.kd_topk_kl_launch_count(T, V, d, K, chunk)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": n,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(w, chunk), parallelism=f"replicas x{world}"),
+        "tflops_nominal": tf_nominal / world,
+        "tflops_algorithmic": flops_alg / (ms_per_step / 1e3) / 1e12,
+        "frac_bf16_peak_burst": tf_nominal / world / burst,
+        "frac_bf16_peak_sustained": tf_nominal / world / sustained,
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "roofline": {"kernel": "kd_gemm_kernel<EPI_FWD> via kd_topk_kl_forward (logit GEMM + "
+                               "online lse + gather; the call also runs 3 small kernels)",
+                     "bound": "tensor", "achieved": fwd_tf,
+                     "peak": sustained, "unit": "TFLOP/s", "frac": fwd_tf / sustained,
+                     "peak_kind": f"bf16 sustained, {peak_src}",
+                     "traffic": load_traffic("kd_gemm_kernel<EPI_FWD>")},
+        "memory": {"peak_allocated_bytes": int(peak),
+                   "peak_minus_inputs_bytes": int(peak - base_alloc),
+                   "dense_TxV_bf16_bytes": int(T) * int(V) * 2},
+        "gpu_launches": int((fl + bl) * n),
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    return out
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="b300", choices=["b300", "reference"])
+    ap.add_argument("--workload", default="ctx_32k")
+    ap.add_argument("--chunk", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=64)
+    ap.add_argument("--ref-rows", type=int, default=32)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    from synth import workload
+    w = workload(args.workload)
+    rank, world, local_rank = rank_info()
+
+    if args.impl == "reference":
+        out = run_reference(args, w, world, rank)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+
+    dist_setup(world, "nccl")
+    out = run_ours(args, w, world, rank, local_rank)
+    if rank == 0:
+        if world == 1 and not args.no_cpu:
+            rows = args.cpu_rows
+            sec = oracle_step_seconds(oracle_sample(w, rows))
+            out["cpu_baseline"] = {"value": rows / sec, "unit": "tokens/s", "cores": blas_threads(),
+                                   "kind": "oracle",
+                                   "sample": f"fp64 oracle fwd+bwd on a {rows}-row sample of "
+                                             f"{w.name} (full V, d), {sec:.1f} s"}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,186 @@
+"""Python binding of libkdtopk.so: the fused, chunked top-K KL distillation loss.
+
+Argument marshalling only.  Every step of the loss runs in the library's CUDA
+kernels; PyTorch supplies device memory and the current stream.  There is no
+fallback: if the library is missing or the device is not an sm_103a GPU, the
+calls raise.
+
+The functions keep the C ABI's names (see include/kd_topk_kl.h):
+
+    kd_topk_kl_workspace_size(T, V, d, K, chunk) -> (fwd_bytes, bwd_bytes)
+    kd_topk_kl_forward(h, W, teacher_idx, teacher_logits, valid, tau, chunk,
+                       loss, lse, row_kl=None, gathered_idx=None, ws=..., dev_status=...)
+    kd_topk_kl_backward(h, W, teacher_idx, teacher_logits, valid, tau, chunk,
+                        lse, grad_loss, dh, dW, ws=..., dev_status=...)
+    kd_gemm_bf16_diag(A, B, C, M, N, Kd, a_mn, b_mn, dev_status=...)
+
+plus `TopKKL`, a small helper that allocates outputs and workspace with torch
+and runs forward + backward.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "KD_OK", "KDError", "lib", "library_path", "status_string",
+    "kd_topk_kl_workspace_size", "kd_topk_kl_launch_count", "kd_topk_kl_forward", "kd_topk_kl_backward",
+    "kd_gemm_bf16_diag", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
+]
+
+KD_OK = 0
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libkdtopk.so")
+
+
+class KDError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} (code {code})")
+        self.code = code
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkdtopk.so (built by __graft_entry__.build() / _build.py)."""
+    global _LIB
+    if _LIB is None:
+        path = library_path()
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing; build it with python -m chunked_top_kl_logit_b300._build")
+        L = ctypes.CDLL(path)
+        i64, i32, f32, vp, sz = ctypes.c_int64, ctypes.c_int32, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+        L.kd_topk_kl_workspace_size.argtypes = [i64, i64, i64, i32, i64, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+        L.kd_topk_kl_workspace_size.restype = ctypes.c_int
+        L.kd_topk_kl_launch_count.argtypes = [i64, i64, i64, i32, i64, ctypes.POINTER(i32),
+                                               ctypes.POINTER(i32)]
+        L.kd_topk_kl_launch_count.restype = ctypes.c_int
+        L.kd_topk_kl_forward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, f32, i64,
+                                         vp, vp, vp, vp, vp, sz, vp, vp]
+        L.kd_topk_kl_forward.restype = ctypes.c_int
+        L.kd_topk_kl_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, f32, i64,
+                                          vp, f32, vp, vp, vp, sz, vp, vp]
+        L.kd_topk_kl_backward.restype = ctypes.c_int
+        L.kd_topk_kl_status_string.argtypes = [ctypes.c_int]
+        L.kd_topk_kl_status_string.restype = ctypes.c_char_p
+        L.kd_gemm_bf16_diag.argtypes = [vp, vp, vp, i64, i64, i64, i32, i32, vp, vp]
+        L.kd_gemm_bf16_diag.restype = ctypes.c_int
+        L.kd_pipeline_wait_selftest.argtypes = [ctypes.c_uint64, vp, vp]
+        L.kd_pipeline_wait_selftest.restype = ctypes.c_int
+        _LIB = L
+    return _LIB
+
+
+def status_string(code: int) -> str:
+    return lib().kd_topk_kl_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch.Tensor")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != KD_OK:
+        raise KDError(rc, where)
+
+
+def kd_topk_kl_workspace_size(T: int, V: int, d: int, K: int, chunk: int):
+    f, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib().kd_topk_kl_workspace_size(T, V, d, K, chunk, ctypes.byref(f), ctypes.byref(b)),
+           "kd_topk_kl_workspace_size")
+    return f.value, b.value
+
+
+def kd_topk_kl_launch_count(T: int, V: int, d: int, K: int, chunk: int):
+    f, b = ctypes.c_int32(0), ctypes.c_int32(0)
+    _check(lib().kd_topk_kl_launch_count(T, V, d, K, chunk, ctypes.byref(f), ctypes.byref(b)),
+           "kd_topk_kl_launch_count")
+    return f.value, b.value
+
+
+def kd_topk_kl_forward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, loss, lse,
+                       row_kl=None, gathered_idx=None, *, ws, dev_status, stream=None):
+    T, d = h.shape
+    V = W.shape[0]
+    K = teacher_idx.shape[1]
+    rc = lib().kd_topk_kl_forward(_ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits),
+                                  _ptr(valid), T, V, d, K, float(tau), int(chunk), _ptr(loss),
+                                  _ptr(lse), _ptr(row_kl), _ptr(gathered_idx), _ptr(ws),
+                                  ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    _check(rc, "kd_topk_kl_forward")
+
+
+def kd_topk_kl_backward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, lse, grad_loss,
+                        dh, dW, *, ws, dev_status, stream=None):
+    T, d = h.shape
+    V = W.shape[0]
+    K = teacher_idx.shape[1]
+    rc = lib().kd_topk_kl_backward(_ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits),
+                                   _ptr(valid), T, V, d, K, float(tau), int(chunk), _ptr(lse),
+                                   float(grad_loss), _ptr(dh), _ptr(dW), _ptr(ws),
+                                   ws.numel() * ws.element_size(), _ptr(dev_status),
+                                   _stream(stream))
+    _check(rc, "kd_topk_kl_backward")
+
+
+def kd_gemm_bf16_diag(A, B, C, M, N, Kd, a_mn, b_mn, *, dev_status, stream=None):
+    rc = lib().kd_gemm_bf16_diag(_ptr(A), _ptr(B), _ptr(C), M, N, Kd, int(a_mn), int(b_mn),
+                                 _ptr(dev_status), _stream(stream))
+    _check(rc, "kd_gemm_bf16_diag")
+
+
+def kd_pipeline_wait_selftest(limit_ns, *, dev_status, stream=None):
+    rc = lib().kd_pipeline_wait_selftest(int(limit_ns), _ptr(dev_status), _stream(stream))
+    _check(rc, "kd_pipeline_wait_selftest")
+
+
+def check_device_status(dev_status, where: str = "device"):
+    """Synchronise-read the device status word and raise if it holds an error."""
+    code = int(dev_status.item())
+    if code != KD_OK:
+        raise KDError(code, where)
+
+
+class TopKKL:
+    """Allocates outputs and one workspace (torch) for a fixed shape and runs
+    the library's forward and backward on the current stream."""
+
+    def __init__(self, T, V, d, K, chunk, device="cuda"):
+        self.T, self.V, self.d, self.K, self.chunk = T, V, d, K, chunk
+        fwd, bwd = kd_topk_kl_workspace_size(T, V, d, K, chunk)
+        dev = torch.device(device)
+        self.ws = torch.empty(max(fwd, bwd), dtype=torch.uint8, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.loss = torch.empty(1, dtype=torch.float32, device=dev)
+        self.lse = torch.empty(T, dtype=torch.float32, device=dev)
+        self.row_kl = torch.empty(T, dtype=torch.float32, device=dev)
+        self.dh = torch.empty(T, d, dtype=torch.float32, device=dev)
+        self.dW = torch.empty(V, d, dtype=torch.float32, device=dev)
+
+    def forward(self, h, W, idx, tl, valid, tau, gathered_idx=None, row_kl=True, stream=None):
+        kd_topk_kl_forward(h, W, idx, tl, valid, tau, self.chunk, self.loss, self.lse,
+                           self.row_kl if row_kl else None, gathered_idx, ws=self.ws,
+                           dev_status=self.status, stream=stream)
+        return self.loss
+
+    def backward(self, h, W, idx, tl, valid, tau, grad_loss=1.0, stream=None):
+        kd_topk_kl_backward(h, W, idx, tl, valid, tau, self.chunk, self.lse, grad_loss,
+                            self.dh, self.dW, ws=self.ws, dev_status=self.status, stream=stream)
+        return self.dh, self.dW

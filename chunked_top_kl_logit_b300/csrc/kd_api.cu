@@ -1,0 +1,458 @@
+// C ABI of the fused top-K KL loss: argument checks, workspace layout,
+// TMA tensor maps and the launch sequence.  The library owns no memory; every
+// buffer (inputs, outputs, workspace, status word) belongs to the caller.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/kd_topk_kl.h"
+#include "kd_kernels.cuh"
+
+using namespace kd;
+
+namespace {
+
+// Split-K and tile-order choices are made for this many SMs (B300) rather
+// than the SM count of whatever device is current, so that results do not
+// depend on the device's SM count.  Grid sizes do use the live SM count.
+constexpr int kPolicySMs = 148;
+constexpr int kRasterGroupRows = 32;  // m tiles per raster group (4096 rows of h in L2)
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// bf16 matrix with `inner` contiguous elements per line, `outer` lines,
+// line pitch `ld` elements; box = 64 inner x box_outer lines, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+              uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int device_sms(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return KD_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return KD_ERR_CUDA;
+  if (major != 10 || minor != 3) return KD_ERR_UNSUPPORTED;
+  return KD_OK;
+}
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int pick_bn(int64_t d) {
+  if (d % 256 == 0) return 256;
+  if (d % 192 == 0) return 192;
+  if (d % 128 == 0) return 128;
+  return 64;
+}
+
+// Split count over the vocabulary for dh = G W: enough (tile, split) units to
+// keep the wave-quantisation loss small, each split at least 32 k-steps long.
+int choose_splits(int64_t tiles, int64_t k_steps) {
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= 8; ++s) {
+    if (s > 1 && k_steps / s < 32) break;
+    const double units = static_cast<double>(tiles) * s;
+    const double eff = units / (std::ceil(units / kPolicySMs) * kPolicySMs);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+    if (eff >= 0.95) break;
+  }
+  return best;
+}
+
+struct Layout {
+  size_t nvalid, losspart, sidx, sp, sslot, tterm;  // shared by both passes
+  size_t zg, part;                                  // forward
+  size_t dz, dhpart;                                // backward
+  size_t fwd_total, bwd_total;
+  int64_t rows_chunk;
+  int bn_d, dh_splits;
+};
+
+Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
+  Layout L{};
+  size_t off = 0;
+  L.nvalid = off;   off += 256;
+  L.losspart = off; off += al256(static_cast<size_t>(cdiv(T, 256)) * 8);
+  L.sidx = off;     off += al256(static_cast<size_t>(T * K) * 4);
+  L.sp = off;       off += al256(static_cast<size_t>(T * K) * 4);
+  L.sslot = off;    off += al256(static_cast<size_t>(T * K) * 2);
+  L.tterm = off;    off += al256(static_cast<size_t>(T) * 4);
+  const size_t common = off;
+  L.zg = off;       off += al256(static_cast<size_t>(T * K) * 4);
+  L.part = off;     off += al256(static_cast<size_t>(cdiv(V, ZBN) * T) * 4);
+  L.fwd_total = off;
+  L.rows_chunk = chunk < T ? chunk : T;
+  L.bn_d = pick_bn(d);
+  L.dh_splits = choose_splits(cdiv(L.rows_chunk, BM) * (d / L.bn_d), cdiv(V, BK));
+  off = common;
+  L.dz = off;       off += al256(static_cast<size_t>(L.rows_chunk * V) * 2);
+  L.dhpart = off;   off += al256(static_cast<size_t>(L.dh_splits - 1) * L.rows_chunk * d * 4);
+  L.bwd_total = off;
+  return L;
+}
+
+int check_shape(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk) {
+  if (T < 1 || V < 1 || d < 1 || K < 1 || chunk < 1) return KD_ERR_INVALID_ARG;
+  if (T > INT32_MAX || V > INT32_MAX || d > INT32_MAX || chunk > INT32_MAX)
+    return KD_ERR_UNSUPPORTED;
+  if (V % 8 != 0 || d % 64 != 0 || K > V || K > 32767) return KD_ERR_UNSUPPORTED;
+  if (static_cast<double>(T) * K > 2e9) return KD_ERR_UNSUPPORTED;
+  return KD_OK;
+}
+
+int check_inputs(const void* h, const void* W, const int32_t* idx, const float* tl,
+                 const uint8_t* valid, int64_t T, int64_t V, int64_t d, int32_t K, float tau,
+                 int64_t chunk, const void* ws, const int32_t* dev_status) {
+  if (!h || !W || !idx || !tl || !valid || !ws || !dev_status) return KD_ERR_INVALID_ARG;
+  if (!(tau > 0.f) || !std::isfinite(tau)) return KD_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws)) return KD_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(idx) & 3u) || (reinterpret_cast<uintptr_t>(tl) & 3u) ||
+      (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+    return KD_ERR_INVALID_ARG;
+  return check_shape(T, V, d, K, chunk);
+}
+
+GemmParams base_params(int a_mn, int b_mn, int BN) {
+  GemmParams p{};
+  p.a_mn = a_mn;
+  p.b_mn = b_mn;
+  p.BN = BN;
+  p.a_bytes = BM * BK * 2;
+  p.b_bytes = static_cast<uint32_t>(BN) * BK * 2;
+  p.stage_bytes = p.a_bytes + p.b_bytes;
+  p.stages = static_cast<int>((200u * 1024u) / p.stage_bytes);
+  if (p.stages > MAX_STAGES) p.stages = MAX_STAGES;
+  p.idesc = make_idesc_bf16(BM, BN, a_mn, b_mn);
+  p.splits = 1;
+  return p;
+}
+
+template <int MODE>
+int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, GemmParams p, int sms,
+                cudaStream_t st) {
+  if (p.num_tiles <= 0) return KD_OK;
+  const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + 256;
+  if (cudaFuncSetAttribute(kd_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return KD_ERR_CUDA;
+  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+  kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
+  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+struct Ws {
+  int* nvalid;
+  double* losspart;
+  int* sidx;
+  float* sp;
+  int16_t* sslot;
+  float* tterm;
+};
+
+Ws carve(void* ws, const Layout& L) {
+  char* w = static_cast<char*>(ws);
+  return Ws{reinterpret_cast<int*>(w + L.nvalid), reinterpret_cast<double*>(w + L.losspart),
+            reinterpret_cast<int*>(w + L.sidx),   reinterpret_cast<float*>(w + L.sp),
+            reinterpret_cast<int16_t*>(w + L.sslot), reinterpret_cast<float*>(w + L.tterm)};
+}
+
+int run_prep(const int32_t* idx, const float* tl, const uint8_t* valid, int64_t T, int32_t K,
+             int64_t V, float inv_tau, const Ws& w, int32_t* dev_status, cudaStream_t st) {
+  if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
+  if (cudaMemsetAsync(w.nvalid, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
+  const int rows_per_block = 8;
+  kd_prep_kernel<<<static_cast<unsigned>(cdiv(T, rows_per_block)), 32 * rows_per_block, 0, st>>>(
+      idx, tl, valid, static_cast<int>(T), K, static_cast<int>(V), inv_tau, w.sidx, w.sp, w.sslot,
+      w.tterm, w.nvalid, dev_status);
+  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+// Logit-tile schedule shared by the forward and the backward recompute.
+void logit_schedule(GemmParams& p, int64_t rows, int64_t V, int64_t d) {
+  p.m_tiles = static_cast<int>(cdiv(rows, BM));
+  p.n_tiles = static_cast<int>(cdiv(V, ZBN));
+  p.num_tiles = p.m_tiles * p.n_tiles;
+  p.k_steps = static_cast<int>(d / BK);
+  p.ks_per_split = p.k_steps;
+  p.group_m = p.m_tiles < kRasterGroupRows ? p.m_tiles : kRasterGroupRows;
+  p.n_fast = 0;
+  p.M = static_cast<int>(rows);
+  p.N = static_cast<int>(V);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kd_topk_kl_status_string(int status) {
+  switch (status) {
+    case KD_OK: return "ok";
+    case KD_ERR_INVALID_ARG: return "invalid argument";
+    case KD_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case KD_ERR_WORKSPACE: return "workspace too small";
+    case KD_ERR_CUDA: return "CUDA call failed";
+    case KD_ERR_INDEX_RANGE: return "teacher index outside [0, V)";
+    case KD_ERR_TIMEOUT: return "bounded pipeline wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int kd_topk_kl_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk,
+                              size_t* fwd_bytes, size_t* bwd_bytes) {
+  const int rc = check_shape(T, V, d, K, chunk);
+  if (rc != KD_OK) return rc;
+  const Layout L = make_layout(T, V, d, K, chunk);
+  if (fwd_bytes) *fwd_bytes = L.fwd_total;
+  if (bwd_bytes) *bwd_bytes = L.bwd_total;
+  return KD_OK;
+}
+
+int kd_topk_kl_launch_count(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk,
+                            int32_t* fwd_launches, int32_t* bwd_launches) {
+  const int rc = check_shape(T, V, d, K, chunk);
+  if (rc != KD_OK) return rc;
+  const Layout L = make_layout(T, V, d, K, chunk);
+  const int64_t chunks = cdiv(T, L.rows_chunk);
+  if (fwd_launches) *fwd_launches = 4;  // prep, logit GEMM, combine, loss
+  if (bwd_launches)
+    *bwd_launches = static_cast<int32_t>(1 + chunks * (L.dh_splits > 1 ? 4 : 3));
+  return KD_OK;
+}
+
+int kd_topk_kl_forward(const void* h, const void* W, const int32_t* teacher_idx,
+                       const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
+                       int64_t d, int32_t K, float tau, int64_t chunk, float* loss, float* lse,
+                       float* row_kl, int32_t* gathered_idx, void* ws, size_t ws_bytes,
+                       int32_t* dev_status, struct CUstream_st* stream) {
+  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
+                        dev_status);
+  if (rc != KD_OK) return rc;
+  if (!loss || !lse) return KD_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, V, d, K, chunk);
+  if (ws_bytes < L.fwd_total) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Ws w = carve(ws, L);
+  char* wb = static_cast<char*>(ws);
+  float* zg = reinterpret_cast<float*>(wb + L.zg);
+  float* part = reinterpret_cast<float*>(wb + L.part);
+  const float inv_tau = 1.0f / tau;
+
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, inv_tau, w, dev_status, st)))
+    return rc;
+
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, h, d, T, d, BM) || !make_map(&tb, W, d, V, d, ZBN)) return KD_ERR_CUDA;
+  GemmParams p = base_params(0, 0, ZBN);
+  logit_schedule(p, T, V, d);
+  p.status = dev_status;
+  p.row0 = 0;
+  p.K = K;
+  p.sidx = w.sidx;
+  p.sp = w.sp;
+  p.sslot = w.sslot;
+  p.inv_tau = inv_tau;
+  p.c_log2 = LOG2E * inv_tau;
+  p.part_ld = T;
+  p.part = part;
+  p.zg = zg;
+  p.gidx = gathered_idx;
+  if ((rc = launch_gemm<EPI_FWD>(ta, tb, p, sms, st))) return rc;
+
+  const int nb = static_cast<int>(cdiv(T, 256));
+  kd_combine_kernel<<<nb, 256, 0, st>>>(part, p.n_tiles, static_cast<int>(T), K, w.sp, zg,
+                                        w.tterm, valid, lse, row_kl, w.losspart);
+  kd_loss_final_kernel<<<1, 256, 0, st>>>(w.losspart, nb, w.nvalid, loss);
+  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx,
+                        const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
+                        int64_t d, int32_t K, float tau, int64_t chunk, const float* lse,
+                        float grad_loss, float* dh, float* dW, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, struct CUstream_st* stream) {
+  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
+                        dev_status);
+  if (rc != KD_OK) return rc;
+  if (!lse || !dh || !dW || !aligned16(dh) || !aligned16(dW)) return KD_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_loss)) return KD_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, V, d, K, chunk);
+  if (ws_bytes < L.bwd_total) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Ws w = carve(ws, L);
+  char* wb = static_cast<char*>(ws);
+  __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(wb + L.dz);
+  float* dhpart = reinterpret_cast<float*>(wb + L.dhpart);
+  const float inv_tau = 1.0f / tau;
+  const int BN = L.bn_d;
+  const int S = L.dh_splits;
+  const __nv_bfloat16* hb = static_cast<const __nv_bfloat16*>(h);
+
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, inv_tau, w, dev_status, st)))
+    return rc;
+
+  for (int64_t c0 = 0; c0 < T; c0 += L.rows_chunk) {
+    const int64_t rows = (T - c0) < L.rows_chunk ? (T - c0) : L.rows_chunk;
+    const __nv_bfloat16* hc = hb + c0 * d;
+    CUtensorMap ta, tb;
+
+    // (1) recompute the chunk's logit tiles and write G as bf16
+    if (!make_map(&ta, hc, d, rows, d, BM) || !make_map(&tb, W, d, V, d, ZBN)) return KD_ERR_CUDA;
+    GemmParams p = base_params(0, 0, ZBN);
+    logit_schedule(p, rows, V, d);
+    p.status = dev_status;
+    p.row0 = static_cast<int>(c0);
+    p.K = K;
+    p.sidx = w.sidx;
+    p.sp = w.sp;
+    p.sslot = w.sslot;
+    p.inv_tau = inv_tau;
+    p.c_log2 = LOG2E * inv_tau;
+    p.lse = lse;
+    p.valid = valid;
+    p.nvalid = w.nvalid;
+    p.grad_loss = grad_loss;
+    p.dz = dz;
+    p.dz_ld = V;
+    if ((rc = launch_gemm<EPI_DZ>(ta, tb, p, sms, st))) return rc;
+
+    // (2) dh rows of the chunk = G W, contraction over V split S ways
+    if (!make_map(&ta, dz, V, rows, V, BM) || !make_map(&tb, W, d, V, d, 64)) return KD_ERR_CUDA;
+    GemmParams q = base_params(0, 1, BN);
+    q.m_tiles = static_cast<int>(cdiv(rows, BM));
+    q.n_tiles = static_cast<int>(d / BN);
+    q.splits = S;
+    q.num_tiles = q.m_tiles * q.n_tiles * S;
+    q.k_steps = static_cast<int>(cdiv(V, BK));
+    q.ks_per_split = static_cast<int>(cdiv(q.k_steps, S));
+    q.n_fast = 1;
+    q.group_m = 1;
+    q.M = static_cast<int>(rows);
+    q.N = static_cast<int>(d);
+    q.status = dev_status;
+    q.out = dh + c0 * d;
+    q.out2 = dhpart;
+    q.ld_out = d;
+    q.split_stride = rows * d;
+    q.accumulate = 0;
+    if ((rc = launch_gemm<EPI_STORE>(ta, tb, q, sms, st))) return rc;
+    if (S > 1) {
+      const int64_t n4 = rows * d / 4;
+      const unsigned blocks = static_cast<unsigned>(sms) * 4;
+      kd_split_reduce_kernel<<<blocks, 256, 0, st>>>(dh + c0 * d, dhpart, S - 1, n4, rows * d);
+      if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+    }
+
+    // (3) dW (+)= G^T h_c, contraction over the chunk's rows
+    if (!make_map(&ta, dz, V, rows, V, 64) || !make_map(&tb, hc, d, rows, d, 64)) return KD_ERR_CUDA;
+    GemmParams r = base_params(1, 1, BN);
+    r.m_tiles = static_cast<int>(cdiv(V, BM));
+    r.n_tiles = static_cast<int>(d / BN);
+    r.num_tiles = r.m_tiles * r.n_tiles;
+    r.k_steps = static_cast<int>(cdiv(rows, BK));
+    r.ks_per_split = r.k_steps;
+    r.n_fast = 1;
+    r.group_m = 1;
+    r.M = static_cast<int>(V);
+    r.N = static_cast<int>(d);
+    r.status = dev_status;
+    r.out = dW;
+    r.out2 = nullptr;
+    r.ld_out = d;
+    r.accumulate = c0 > 0 ? 1 : 0;
+    if ((rc = launch_gemm<EPI_STORE>(ta, tb, r, sms, st))) return rc;
+  }
+  return KD_OK;
+}
+
+int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t Kd,
+                      int32_t a_mn, int32_t b_mn, int32_t* dev_status,
+                      struct CUstream_st* stream) {
+  if (!A || !B || !C || !dev_status) return KD_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || Kd < 1 || (a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1))
+    return KD_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return KD_ERR_INVALID_ARG;
+  if (M % 8 || N % 8 || Kd % 8 || M > INT32_MAX || N > INT32_MAX || Kd > INT32_MAX)
+    return KD_ERR_UNSUPPORTED;
+  int sms = 0;
+  int rc = device_sms(&sms);
+  if (rc != KD_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int BN = N >= 256 ? 256 : static_cast<int>(cdiv(N, 64) * 64);
+  CUtensorMap ta, tb;
+  const bool okA = a_mn ? make_map(&ta, A, M, Kd, M, 64) : make_map(&ta, A, Kd, M, Kd, BM);
+  const bool okB = b_mn ? make_map(&tb, B, N, Kd, N, 64) : make_map(&tb, B, Kd, N, Kd, BN);
+  if (!okA || !okB) return KD_ERR_CUDA;
+  GemmParams p = base_params(a_mn, b_mn, BN);
+  p.m_tiles = static_cast<int>(cdiv(M, BM));
+  p.n_tiles = static_cast<int>(cdiv(N, BN));
+  p.num_tiles = p.m_tiles * p.n_tiles;
+  p.k_steps = static_cast<int>(cdiv(Kd, BK));
+  p.ks_per_split = p.k_steps;
+  p.n_fast = 1;
+  p.group_m = 1;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.status = dev_status;
+  p.out = C;
+  p.ld_out = N;
+  if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
+  return launch_gemm<EPI_STORE>(ta, tb, p, sms, st);
+}
+
+int kd_pipeline_wait_selftest(uint64_t limit_ns, int32_t* dev_status,
+                              struct CUstream_st* stream) {
+  if (!dev_status || limit_ns == 0 || limit_ns > 1000000000ull) return KD_ERR_INVALID_ARG;
+  int sms = 0;
+  const int rc = device_sms(&sms);
+  if (rc != KD_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
+  kd_wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, dev_status);
+  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+}  // extern "C"

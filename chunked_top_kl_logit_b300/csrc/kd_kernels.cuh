@@ -1,0 +1,621 @@
+// Device kernels of the fused top-K KL loss.
+//
+// The contraction kernel is one persistent, warp-specialised tcgen05 GEMM
+// (tile 128 x BN x 64, bf16 in, fp32 accumulate in TMEM) shared by the four
+// contractions of the method:
+//
+//   forward   z = h W^T tile by tile      -> epilogue EPI_FWD: online log-sum-exp
+//                                            partial per (row, vocab tile) and
+//                                            the gather of z at the row's cached
+//                                            teacher indices
+//   backward  z = h_c W^T again (chunk c) -> epilogue EPI_DZ: G = s (q - scatter p)/tau
+//                                            written as bf16 into the chunk buffer
+//             dh_c = G_c W                -> epilogue EPI_STORE (split over V)
+//             dW  += G_c^T h_c            -> epilogue EPI_STORE (accumulate)
+//
+// Warp roles (192 threads): warp 0 issues TMA loads into a ring of shared
+// memory stages, warp 1 owns TMEM and issues tcgen05.mma from one thread,
+// warps 2..5 drain the two TMEM accumulators (one TMEM lane = one tile row
+// per thread) while the next tile accumulates into the other one.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "kd_ptx.cuh"
+
+namespace kd {
+
+constexpr int BM = 128;            // tile rows = TMEM lanes
+constexpr int BK = 64;             // contraction elements per stage (128 B of bf16)
+constexpr int ZBN = 256;           // logit tile width over the vocabulary
+constexpr int TMEM_COLS = 512;     // two accumulators of up to 256 fp32 columns
+constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int MAX_STAGES = 8;
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+
+enum EpiMode { EPI_FWD = 0, EPI_DZ = 1, EPI_STORE = 2 };
+
+struct GemmParams {
+  // schedule: tile t -> (split s, m tile, n tile)
+  int m_tiles, n_tiles, splits, num_tiles;
+  int k_steps;        // contraction length in steps of BK
+  int ks_per_split;   // steps per split (the last split may be shorter, never empty)
+  int group_m;        // n_fast == 0: m tiles per raster group (n-major inside a group)
+  int n_fast;         // 1: n is the fastest index inside a split
+  // operands
+  int a_mn, b_mn;     // 0: K-major tile, 1: MN-major tile
+  int BN;             // tile width (MMA N)
+  int stages;
+  uint32_t a_bytes, b_bytes, stage_bytes;
+  uint32_t idesc;
+  // epilogue, all modes
+  int M, N;           // valid output rows / columns of this launch
+  int* status;
+  // EPI_STORE: split 0 writes `out`, split s >= 1 writes `out2 + (s-1)*split_stride`
+  float* out;
+  float* out2;
+  int64_t ld_out;
+  int64_t split_stride;
+  int accumulate;     // add into the existing values of `out`
+  // EPI_FWD / EPI_DZ (per-row tables are indexed by the global row row0 + local row)
+  int row0;
+  int K;
+  const int* sidx;        // [T][K] teacher indices, ascending per row
+  const float* sp;        // [T][K] teacher probabilities in the same order
+  const int16_t* sslot;   // [T][K] original slot of each sorted entry
+  float inv_tau;          // 1 / tau
+  float c_log2;           // log2(e) / tau
+  int64_t part_ld;        // row stride (= T) of the partial table
+  float* part;            // [n_tiles][T] natural-log lse of each vocabulary tile
+  float* zg;              // [T][K] z / tau gathered at the sorted entries
+  int* gidx;              // [T][K] (slot order) vocabulary column read, or null
+  const float* lse;       // [T]
+  const uint8_t* valid;   // [T]
+  const int* nvalid;      // device scalar
+  float grad_loss;
+  __nv_bfloat16* dz;      // [rows][dz_ld] chunk buffer
+  int64_t dz_ld;
+};
+
+struct TileCoord {
+  int m, n, s;
+};
+
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
+  const int per_split = p.m_tiles * p.n_tiles;
+  TileCoord c;
+  c.s = t / per_split;
+  const int r = t - c.s * per_split;
+  if (p.n_fast) {
+    c.m = r / p.n_tiles;
+    c.n = r - c.m * p.n_tiles;
+  } else {
+    const int gsz = p.group_m * p.n_tiles;
+    const int g = r / gsz;
+    const int m0 = g * p.group_m;
+    const int gm = min(p.group_m, p.m_tiles - m0);
+    const int j = r - g * gsz;
+    c.n = j / gm;
+    c.m = m0 + (j - c.n * gm);
+  }
+  return c;
+}
+
+// First position in the ascending row `s[0..K)` whose value is >= key.
+__device__ __forceinline__ int lower_bound_row(const int* __restrict__ s, int K, int key) {
+  int lo = 0, hi = K;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(s + mid) < key) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
+// ------------------------------------------------------------------ roles
+
+__device__ __forceinline__ void producer_role(const GemmParams& p, const CUtensorMap* tmA,
+                                              const CUtensorMap* tmB, uint8_t* smem,
+                                              uint64_t* full, uint64_t* empty,
+                                              volatile int* abort_flag) {
+  tma_prefetch_desc(tmA);
+  tma_prefetch_desc(tmB);
+  int stage = 0;
+  uint32_t phase = 0;
+  int issued = 0;
+  bool ok = true;
+  for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+    const TileCoord c = decode_tile(p, t);
+    const int kb = c.s * p.ks_per_split;
+    const int ke = min(p.k_steps, kb + p.ks_per_split);
+    for (int ks = kb; ks < ke; ++ks) {
+      if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+      uint8_t* sa = smem + static_cast<size_t>(stage) * p.stage_bytes;
+      uint8_t* sb = sa + p.a_bytes;
+      mbar_arrive_expect_tx(&full[stage], p.stage_bytes);
+      const int k0 = ks * BK;
+      if (!p.a_mn) {
+        tma_load_2d(sa, tmA, &full[stage], k0, c.m * BM);
+      } else {
+        tma_load_2d(sa, tmA, &full[stage], c.m * BM, k0);
+        tma_load_2d(sa + 8192, tmA, &full[stage], c.m * BM + 64, k0);
+      }
+      if (!p.b_mn) {
+        tma_load_2d(sb, tmB, &full[stage], k0, c.n * p.BN);
+      } else {
+        for (int j = 0; j < p.BN / 64; ++j)
+          tma_load_2d(sb + j * 8192, tmB, &full[stage], c.n * p.BN + 64 * j, k0);
+      }
+      ++issued;
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+  }
+  if (!ok) {
+    // let the loads this thread started land before the CTA leaves
+    for (int i = max(0, issued - p.stages); i < issued; ++i)
+      mbar_wait_drain(&full[i % p.stages], static_cast<uint32_t>((i / p.stages) & 1));
+  }
+}
+
+__device__ __forceinline__ void mma_role(const GemmParams& p, uint8_t* smem, uint64_t* full,
+                                         uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
+                                         uint64_t* drain, uint32_t tmem_base,
+                                         volatile int* abort_flag) {
+  const uint32_t a_lbo = p.a_mn ? 8192u : 16u;
+  const uint32_t b_lbo = p.b_mn ? 8192u : 16u;
+  const uint32_t a_adv = p.a_mn ? 2048u : 32u;  // bytes per 16-element K step
+  const uint32_t b_adv = p.b_mn ? 2048u : 32u;
+  const uint32_t smem0 = smem_u32(smem);
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  int lt = 0;
+  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
+    const TileCoord c = decode_tile(p, t);
+    const int kb = c.s * p.ks_per_split;
+    const int ke = min(p.k_steps, kb + p.ks_per_split);
+    const int acc = lt & 1;
+    const uint32_t use = static_cast<uint32_t>(lt >> 1);
+    if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) { ok = false; break; }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
+    for (int ks = kb; ks < ke; ++ks) {
+      if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t sa = smem0 + static_cast<uint32_t>(stage) * p.stage_bytes;
+      const uint32_t sb = sa + p.a_bytes;
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        const uint64_t ad = make_sdesc(sa + kk * a_adv, a_lbo, 1024u);
+        const uint64_t bd = make_sdesc(sb + kk * b_adv, b_lbo, 1024u);
+        umma_bf16(d_tmem, ad, bd, p.idesc, (ks > kb || kk > 0) ? 1u : 0u);
+      }
+      umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
+      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
+    }
+    if (!ok) break;
+    umma_commit(&tfull[acc]);      // accumulator ready for the epilogue
+  }
+  if (!ok) {
+    umma_commit(drain);
+    mbar_wait_drain(drain, 0);
+  }
+}
+
+// ------------------------------------------------------------------ epilogues
+
+// Forward: per (row, vocab tile) natural-log lse partial of z/tau and the
+// gather of z/tau at the row's cached indices that fall inside the tile.
+__device__ __forceinline__ void epi_fwd(const GemmParams& p, const TileCoord& c, int acc,
+                                        uint32_t tmem_row, int r_in_tile, uint64_t* tfull,
+                                        uint64_t* tempty, uint32_t use, volatile int* abort_flag,
+                                        bool& ok) {
+  const int lrow = c.m * BM + r_in_tile;
+  const bool row_ok = lrow < p.M;
+  const int64_t grow = static_cast<int64_t>(p.row0) + lrow;
+  const int v0 = c.n * ZBN;
+  const int* srow = p.sidx + grow * p.K;
+  int pos = p.K;
+  int nxt = INT_MAX;
+  if (row_ok) {  // start of this row's entries inside the tile (overlaps the MMA)
+    pos = lower_bound_row(srow, p.K, v0);
+    nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
+  }
+  bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
+  ok = __all_sync(0xffffffffu, w);
+  if (!ok) return;
+  tc_fence_after();
+  float m = -CUDART_INF_F;
+  float s = 0.f;
+#pragma unroll 1
+  for (int cc = 0; cc < ZBN / 32; ++cc) {
+    const int cb = v0 + cc * 32;
+    if (cb >= p.N) break;  // uniform: depends on the tile only
+    uint32_t r[32];
+    tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
+    tmem_ld_wait(r);
+    float u[32];
+    float cm = -CUDART_INF_F;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      u[j] = (cb + j < p.N) ? __uint_as_float(r[j]) * p.c_log2 : -CUDART_INF_F;
+      cm = fmaxf(cm, u[j]);
+    }
+    const float mn = fmaxf(m, cm);
+    float cs = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cs += ex2f(u[j] - mn);
+    s = s * ex2f(m - mn) + cs;
+    m = mn;
+    const int ce = cb + 32;
+    while (__any_sync(0xffffffffu, nxt < ce)) {
+      if (nxt < ce) {
+        const int j = nxt - cb;
+        uint32_t bits = 0;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) bits = (jj == j) ? r[jj] : bits;
+        p.zg[grow * p.K + pos] = __uint_as_float(bits) * p.inv_tau;
+        if (p.gidx) p.gidx[grow * p.K + p.sslot[grow * p.K + pos]] = nxt;
+        ++pos;
+        nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
+      }
+    }
+  }
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
+  if (row_ok) p.part[static_cast<int64_t>(c.n) * p.part_ld + grow] = (m + lg2f(s)) * LN2;
+}
+
+// Backward: G = s_t (exp(z/tau - lse) - scatter p) / tau as bf16 into the chunk buffer.
+__device__ __forceinline__ void epi_dz(const GemmParams& p, const TileCoord& c, int acc,
+                                       uint32_t tmem_row, int r_in_tile, uint64_t* tfull,
+                                       uint64_t* tempty, uint32_t use, volatile int* abort_flag,
+                                       bool& ok) {
+  const int lrow = c.m * BM + r_in_tile;
+  const bool row_ok = lrow < p.M;
+  const int64_t grow = static_cast<int64_t>(p.row0) + lrow;
+  const int v0 = c.n * ZBN;
+  const int* srow = p.sidx + grow * p.K;
+  float sc = 0.f;   // g * valid / N_valid / tau
+  float lb = 0.f;   // lse in base 2
+  int pos = p.K;
+  int nxt = INT_MAX;
+  if (row_ok) {
+    const int nv = *p.nvalid;
+    if (p.valid[grow] && nv > 0) {
+      sc = p.grad_loss / static_cast<float>(nv) * p.inv_tau;
+      lb = p.lse[grow] * LOG2E;
+      pos = lower_bound_row(srow, p.K, v0);
+      nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
+    }
+  }
+  bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
+  ok = __all_sync(0xffffffffu, w);
+  if (!ok) return;
+  tc_fence_after();
+  __nv_bfloat16* drow = p.dz + static_cast<int64_t>(lrow) * p.dz_ld;
+#pragma unroll 1
+  for (int cc = 0; cc < ZBN / 32; ++cc) {
+    const int cb = v0 + cc * 32;
+    if (cb >= p.N) break;
+    uint32_t r[32];
+    tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
+    tmem_ld_wait(r);
+    float g[32];
+    if (sc != 0.f) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] = sc * ex2f(__uint_as_float(r[j]) * p.c_log2 - lb);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) g[j] = 0.f;
+    }
+    const int ce = cb + 32;
+    while (__any_sync(0xffffffffu, nxt < ce)) {
+      if (nxt < ce) {
+        const int j = nxt - cb;
+        const float dp = sc * __ldg(p.sp + grow * p.K + pos);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) g[jj] = (jj == j) ? g[jj] - dp : g[jj];
+        ++pos;
+        nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
+      }
+    }
+    if (row_ok) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (cb + 8 * q < p.N) {
+          uint4 pk;
+          __nv_bfloat162 b0 = __floats2bfloat162_rn(g[8 * q + 0], g[8 * q + 1]);
+          __nv_bfloat162 b1 = __floats2bfloat162_rn(g[8 * q + 2], g[8 * q + 3]);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(g[8 * q + 4], g[8 * q + 5]);
+          __nv_bfloat162 b3 = __floats2bfloat162_rn(g[8 * q + 6], g[8 * q + 7]);
+          pk.x = *reinterpret_cast<uint32_t*>(&b0);
+          pk.y = *reinterpret_cast<uint32_t*>(&b1);
+          pk.z = *reinterpret_cast<uint32_t*>(&b2);
+          pk.w = *reinterpret_cast<uint32_t*>(&b3);
+          *reinterpret_cast<uint4*>(drow + cb + 8 * q) = pk;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
+}
+
+// fp32 tile store, optionally accumulating into the existing output.
+__device__ __forceinline__ void epi_store(const GemmParams& p, const TileCoord& c, int acc,
+                                          uint32_t tmem_row, int r_in_tile, uint64_t* tfull,
+                                          uint64_t* tempty, uint32_t use,
+                                          volatile int* abort_flag, bool& ok) {
+  const int row = c.m * BM + r_in_tile;
+  const bool row_ok = row < p.M;
+  const int n0 = c.n * p.BN;
+  float* orow = (c.s == 0 ? p.out : p.out2 + static_cast<int64_t>(c.s - 1) * p.split_stride) +
+                static_cast<int64_t>(row) * p.ld_out;
+  const bool accum = p.accumulate && c.s == 0;
+  bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
+  ok = __all_sync(0xffffffffu, w);
+  if (!ok) return;
+  tc_fence_after();
+#pragma unroll 1
+  for (int cc = 0; cc < p.BN / 32; ++cc) {
+    const int cb = n0 + cc * 32;
+    if (cb >= p.N) break;
+    uint32_t r[32];
+    tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
+    tmem_ld_wait(r);
+    if (row_ok) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int col = cb + 4 * q;
+        if (col < p.N) {
+          float4 v = make_float4(__uint_as_float(r[4 * q + 0]), __uint_as_float(r[4 * q + 1]),
+                                 __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+          float4* dst = reinterpret_cast<float4*>(orow + col);
+          if (accum) {
+            const float4 o = *dst;
+            v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+          }
+          *dst = v;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
+  uint64_t* empty = full + MAX_STAGES;
+  uint64_t* tfull = empty + MAX_STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) producer_role(p, &tmA, &tmB, smem, full, empty, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) mma_role(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int r_in_tile = q * 32 + lane;
+    const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    bool ok = true;
+    int lt = 0;
+    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
+      const TileCoord c = decode_tile(p, t);
+      const int acc = lt & 1;
+      const uint32_t use = static_cast<uint32_t>(lt >> 1);
+      if (MODE == EPI_FWD)
+        epi_fwd(p, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+      else if (MODE == EPI_DZ)
+        epi_dz(p, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+      else
+        epi_store(p, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+      if (!ok) break;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------ SIMT kernels
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Teacher side of each row, one warp per row: range check of the cached
+// indices, p = softmax(teacher_logits / tau) over the K entries, the teacher
+// term sum_k p log p, and the entries sorted by vocabulary index (ties keep
+// slot order) so that the contraction epilogues can walk them tile by tile.
+__global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restrict__ tl,
+                               const uint8_t* __restrict__ valid, int T, int K, int V,
+                               float inv_tau, int* __restrict__ sidx, float* __restrict__ sp,
+                               int16_t* __restrict__ sslot, float* __restrict__ tterm,
+                               int* __restrict__ nvalid, int* status) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;
+  const int* ir = idx + static_cast<int64_t>(row) * K;
+  const float* tr = tl + static_cast<int64_t>(row) * K;
+  float m = -CUDART_INF_F;
+  int bad = 0;
+  for (int k = lane; k < K; k += 32) {
+    m = fmaxf(m, tr[k] * inv_tau);
+    const int v = ir[k];
+    bad |= (v < 0 || v >= V);
+  }
+  m = warp_max(m);
+  if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, KD_ERR_INDEX_RANGE);
+  float S = 0.f;
+  for (int k = lane; k < K; k += 32) S += expf(tr[k] * inv_tau - m);
+  S = warp_sum(S);
+  const float logS = logf(S);
+  float tt = 0.f;
+  int* so = sidx + static_cast<int64_t>(row) * K;
+  float* po = sp + static_cast<int64_t>(row) * K;
+  int16_t* lo = sslot + static_cast<int64_t>(row) * K;
+  for (int k = lane; k < K; k += 32) {
+    const float lp = tr[k] * inv_tau - m - logS;
+    const float pk = expf(lp);
+    if (pk > 0.f) tt += pk * lp;
+    const int v = ir[k];
+    int rank = 0;
+    for (int j = 0; j < K; ++j) {
+      const int u = ir[j];
+      rank += (u < v) || (u == v && j < k);
+    }
+    so[rank] = v;
+    po[rank] = pk;
+    lo[rank] = static_cast<int16_t>(k);
+  }
+  tt = warp_sum(tt);
+  if (lane == 0) {
+    tterm[row] = tt;
+    if (valid[row]) atomicAdd(nvalid, 1);
+  }
+}
+
+// One thread per row: lse from the per-tile partials, row_kl, and a per-block
+// (double) partial sum of row_kl for the deterministic loss reduction.
+__global__ void kd_combine_kernel(const float* __restrict__ part, int n_tiles, int T, int K,
+                                  const float* __restrict__ sp, const float* __restrict__ zg,
+                                  const float* __restrict__ tterm,
+                                  const uint8_t* __restrict__ valid, float* __restrict__ lse_out,
+                                  float* __restrict__ row_kl_out, double* __restrict__ losspart) {
+  __shared__ double red[256];
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  double kl = 0.0;
+  if (row < T) {
+    float m = -CUDART_INF_F;
+    float s = 0.f;
+    for (int j = 0; j < n_tiles; ++j) {
+      const float x = part[static_cast<int64_t>(j) * T + row];
+      if (x > m) {
+        s = s * expf(m - x) + 1.f;
+        m = x;
+      } else {
+        s += expf(x - m);
+      }
+    }
+    const float lse = m + logf(s);
+    lse_out[row] = lse;
+    float rk = 0.f;
+    if (valid[row]) {
+      const float* pr = sp + static_cast<int64_t>(row) * K;
+      const float* zr = zg + static_cast<int64_t>(row) * K;
+      float a = 0.f;
+      for (int k = 0; k < K; ++k) a += pr[k] * (lse - zr[k]);
+      rk = tterm[row] + a;
+    }
+    if (row_kl_out) row_kl_out[row] = rk;
+    kl = rk;
+  }
+  red[threadIdx.x] = kl;
+  __syncthreads();
+  for (int o = blockDim.x >> 1; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) losspart[blockIdx.x] = red[0];
+}
+
+// Single block: fixed-order sum of the per-block partials, divided by N_valid.
+__global__ void kd_loss_final_kernel(const double* __restrict__ losspart, int nb,
+                                     const int* __restrict__ nvalid, float* __restrict__ loss) {
+  __shared__ double red[256];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) s += losspart[i];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = blockDim.x >> 1; o > 0; o >>= 1) {
+    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const int n = *nvalid;
+    *loss = n > 0 ? static_cast<float>(red[0] / n) : 0.f;
+  }
+}
+
+// dh[i] += sum_{s} part[s][i] in a fixed order (split-K completion).
+__global__ void kd_split_reduce_kernel(float* __restrict__ out, const float* __restrict__ part,
+                                       int nparts, int64_t n4, int64_t stride) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float4 a = reinterpret_cast<float4*>(out)[i];
+    for (int s = 0; s < nparts; ++s) {
+      const float4 b = reinterpret_cast<const float4*>(part + s * stride)[i];
+      a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+    }
+    reinterpret_cast<float4*>(out)[i] = a;
+  }
+}
+
+// One thread waits, through the pipeline's bounded wait, on an mbarrier that
+// nothing arrives on; the wait must give up after limit_ns and report
+// KD_ERR_TIMEOUT in *status.
+__global__ void kd_wait_selftest_kernel(uint64_t limit_ns, int* status) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    volatile int* af = &abort_flag;
+    mbar_wait(&bar, 0, af, status, limit_ns);
+  }
+}
+
+}  // namespace kd

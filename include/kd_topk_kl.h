@@ -1,0 +1,164 @@
+/*
+ * kd_topk_kl.h - fused, chunked top-K KL distillation loss on one B300 (sm_103a).
+ *
+ * What it computes.  "Making Knowledge Distillation Cheap Enough to Run at
+ * Scale" (aipuls.nl summary, section "Summary", second paragraph) describes a
+ * teacher whose top-100 logits per token position are cached offline, and a
+ * student trained with a KL-divergence loss that runs as a fused, chunked
+ * kernel which never forms the full sequence-by-vocabulary matrix and keeps
+ * its working memory bounded by one chunk.  The agent-gateway.com news piece
+ * ("Hugging Face and Multiverse Computing cut KD memory costs", paragraphs on
+ * the second bottleneck) restates the chunked, fused evaluation.  The pages
+ * give no formula; this library fixes the following definition:
+ *
+ *   z      = h W^T                       student logits, T x V (never stored)
+ *   lse_t  = log sum_v exp(z_tv / tau)   full-vocabulary log-normaliser
+ *   p_tk   = softmax_k(teacher_logits_tk / tau)   renormalised over the K cached entries
+ *   row_kl_t = valid_t ? sum_k p_tk (log p_tk - (z_t,idx_tk / tau - lse_t)) : 0
+ *   loss   = sum_t row_kl_t / N_valid    (0 when N_valid = 0)
+ *   G_tv   = g (valid_t / N_valid) (exp(z_tv/tau - lse_t) - sum_{k: idx_tk = v} p_tk) / tau
+ *   dh     = G W,  dW = G^T h
+ *
+ * The direction KL(teacher || student) and the mean over valid tokens follow
+ * the dense sketch in the asibiont.com rewrite ("A Concrete Implementation
+ * Sketch").  No tau^2 factor.  Duplicate indices in a row count once per slot.
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers marked "device" are CUDA device pointers on the current device;
+ *    the library never allocates, frees or copies to the host.  The caller
+ *    owns every buffer, including the workspace `ws`.
+ *  - Row-major, contiguous, 16-byte aligned arrays:
+ *      h              bf16 [T x d]
+ *      W              bf16 [V x d]   (nn.Linear weight layout)
+ *      teacher_idx    int32 [T x K]  values in [0, V)
+ *      teacher_logits fp32 [T x K]
+ *      valid          uint8 [T]      nonzero = row takes part in the loss
+ *  - Limits: T >= 1, V >= 1 with V % 8 == 0, d >= 64 with d % 64 == 0,
+ *    1 <= K <= min(V, 32767), tau > 0 and finite, chunk >= 1.  T, V, d, K
+ *    and chunk must each fit in 31 bits.
+ *  - Host-side errors (bad arguments, workspace too small, launch failures)
+ *    are returned synchronously as a kd_status and nothing is launched for
+ *    argument errors.
+ *  - Device-side errors are asynchronous: the kernels write the first error
+ *    (KD_ERR_INDEX_RANGE for a teacher index outside [0, V), KD_ERR_TIMEOUT
+ *    if an internal pipeline wait exceeds its bound) into *dev_status, which
+ *    each call first resets to 0 on `stream`.  Read it after synchronising the
+ *    stream.  Outputs are unspecified when it is nonzero.  The kernels never
+ *    trap.
+ *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ */
+#ifndef KD_TOPK_KL_H_
+#define KD_TOPK_KL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+typedef enum kd_status {
+  KD_OK = 0,
+  KD_ERR_INVALID_ARG = 1,  /* null pointer, bad size, tau <= 0, misalignment */
+  KD_ERR_UNSUPPORTED = 2,  /* no sm_103a device, or shape outside the limits above */
+  KD_ERR_WORKSPACE = 3,    /* ws_bytes smaller than kd_topk_kl_workspace_size() */
+  KD_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+  KD_ERR_INDEX_RANGE = 5,  /* device: a teacher index is outside [0, V) */
+  KD_ERR_TIMEOUT = 6       /* device: a bounded pipeline wait ran out */
+} kd_status;
+
+/*
+ * Workspace bytes for kd_topk_kl_forward (*fwd_bytes) and
+ * kd_topk_kl_backward (*bwd_bytes) at this shape.  Either output pointer may
+ * be NULL.  The forward workspace holds the per-row sorted teacher entries and
+ * one fp32 log-sum-exp partial per (row, 256-column vocabulary tile); the
+ * backward workspace holds the sorted entries and one bf16 gradient chunk of
+ * chunk x V elements (the only buffer whose size depends on V times a row
+ * count: the "memory bounded by a single chunk" of the aipuls.nl summary).
+ * Host-only; returns KD_ERR_INVALID_ARG / KD_ERR_UNSUPPORTED on bad shapes.
+ */
+int kd_topk_kl_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk,
+                              size_t* fwd_bytes, size_t* bwd_bytes);
+
+/*
+ * Number of kernels kd_topk_kl_forward / kd_topk_kl_backward enqueue at this
+ * shape (the status/counter resets are cudaMemsetAsync calls and are not
+ * counted).  Host-only; either output pointer may be NULL.
+ */
+int kd_topk_kl_launch_count(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk,
+                            int32_t* fwd_launches, int32_t* bwd_launches);
+
+/*
+ * Forward: loss, per-row lse, per-row KL (aipuls.nl "Summary": the KL between
+ * the cached teacher top-K and the student, evaluated tile by tile without a
+ * T x V buffer).
+ *
+ * Inputs  (device): h, W, teacher_idx, teacher_logits, valid as above.
+ * Outputs (device): loss     fp32 scalar
+ *                   lse      fp32 [T]   log sum_v exp(z_tv / tau), every row
+ *                   row_kl   fp32 [T]   or NULL; 0 for invalid rows
+ *                   gathered_idx int32 [T x K] or NULL: for every (t, k), the
+ *                            vocabulary column whose logit the kernel read
+ *                            for slot k (diagnostic; equals teacher_idx).
+ * `chunk` is accepted for symmetry with the backward and is not used here:
+ * the forward holds no chunk-sized buffer.
+ * ws/ws_bytes: caller-owned device scratch, at least *fwd_bytes.
+ */
+int kd_topk_kl_forward(const void* h, const void* W, const int32_t* teacher_idx,
+                       const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
+                       int64_t d, int32_t K, float tau, int64_t chunk, float* loss, float* lse,
+                       float* row_kl, int32_t* gathered_idx, void* ws, size_t ws_bytes,
+                       int32_t* dev_status, struct CUstream_st* stream);
+
+/*
+ * Backward: dh = G W and dW = G^T h for the loss above scaled by grad_loss.
+ * Rows are processed in chunks of `chunk` rows: for each chunk the logit tiles
+ * are recomputed, G is written as bf16 into the chunk buffer in `ws`, and two
+ * tensor-core contractions produce that chunk's rows of dh and add its
+ * contribution to dW (the first chunk overwrites dW).
+ *
+ * lse: device fp32 [T] as produced by kd_topk_kl_forward for the same inputs.
+ * Outputs (device): dh fp32 [T x d] (overwritten; rows of invalid tokens are
+ * exactly 0), dW fp32 [V x d] (overwritten).
+ * ws/ws_bytes: caller-owned device scratch, at least *bwd_bytes.  It need not
+ * hold anything from the forward.
+ */
+int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx,
+                        const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
+                        int64_t d, int32_t K, float tau, int64_t chunk, const float* lse,
+                        float grad_loss, float* dh, float* dW, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, struct CUstream_st* stream);
+
+/* Static, NUL-terminated description of a kd_status value (never NULL). */
+const char* kd_topk_kl_status_string(int status);
+
+/*
+ * Diagnostic of the contraction step alone: C = A B^T on the same tcgen05
+ * tensor-core pipeline that produces the logit tiles z = h W^T above, with an
+ * fp32 store epilogue instead of the loss.  C fp32 [M x N] row-major.
+ * a_mn = 0: A is bf16 [M x Kd] row-major (K-major); a_mn = 1: A is given as
+ * bf16 [Kd x M] row-major (M contiguous).  Likewise b_mn for B ([N x Kd] or
+ * [Kd x N]).  Limits: M, N, Kd >= 1 and multiples of 8 (a contraction tail
+ * shorter than 64 is zero-filled by TMA).  Device pointers; stream as above.
+ */
+int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t Kd,
+                      int32_t a_mn, int32_t b_mn, int32_t* dev_status,
+                      struct CUstream_st* stream);
+
+/*
+ * Self-test of the failure detection every pipeline wait relies on (the pages
+ * describe no failure handling; this checks the library's own bound).  One
+ * thread waits on an mbarrier that nothing arrives on, through the same
+ * bounded wait the contraction kernels use; after limit_ns (1 ns .. 1 s) the
+ * wait gives up and the kernel writes KD_ERR_TIMEOUT to *dev_status (device
+ * int32, reset to 0 first) and returns, leaving the context usable.
+ */
+int kd_pipeline_wait_selftest(uint64_t limit_ns, int32_t* dev_status, struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KD_TOPK_KL_H_ */

@@ -163,7 +163,7 @@ def make_inputs(w: Workload, seed: int = 0, device=None) -> dict:
 
     if w.idx_kind == "uniform":
         idx = _distinct_draws(rng, T, K, V, None)
-        tl = np.sort(rng.normal(0.0, 2.0, size=(T, K)).astype(np.float32), axis=1)[:, ::-1]
+        tl = np.sort(rng.normal(0.0, 2.0, size=(T, K)).astype(np.float32), axis=1)[:, ::-1].copy()
     elif w.idx_kind == "teacher":
         n_top = min(20, K)
         if device is None:

@@ -1,0 +1,130 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+public header declares, and rejects bad arguments synchronously with a
+kd_status code before touching CUDA.  The device pointers below are fake,
+16-byte-aligned addresses: the library never dereferences a device pointer on
+the host, and every case here returns before any CUDA call."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import chunked_top_kl_logit_b300 as kd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kd_topk_kl.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA, RANGE, TIMEOUT = range(7)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kd_\w+)\s*\(", text)))
+
+
+def test_header_symbols_exported():
+    names = declared_functions()
+    assert "kd_topk_kl_forward" in names and "kd_topk_kl_backward" in names
+    L = kd.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        getattr(L, n)  # resolves the symbol
+
+
+def test_status_strings():
+    for code in range(7):
+        s = kd.status_string(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert kd.status_string(99) == "unknown status"
+
+
+def test_workspace_sizes():
+    f, b = kd.kd_topk_kl_workspace_size(32768, 201088, 2880, 100, 8192)
+    # forward: one fp32 lse partial per (row, 256-wide vocab tile) dominates
+    assert f >= 32768 * ((201088 + 255) // 256) * 4
+    # backward: the bf16 gradient chunk dominates, bounded by chunk x V
+    assert 8192 * 201088 * 2 <= b < 8192 * 201088 * 2 + 32768 * 100 * 20 + 8192 * 2880 * 4 * 8
+    f1, b1 = kd.kd_topk_kl_workspace_size(32768, 201088, 2880, 100, 2048)
+    assert b1 < b and f1 == f
+
+
+@pytest.mark.parametrize("shape,code", [
+    ((0, 1024, 64, 4, 16), INVALID), ((16, 0, 64, 4, 16), INVALID),
+    ((16, 1024, 0, 4, 16), INVALID), ((16, 1024, 64, 0, 16), INVALID),
+    ((16, 1024, 64, 4, 0), INVALID), ((16, 1020, 64, 4, 16), UNSUPPORTED),
+    ((16, 1024, 96, 4, 16), UNSUPPORTED), ((16, 1024, 64, 1025, 16), UNSUPPORTED),
+    ((16, 65536, 64, 40000, 16), UNSUPPORTED), ((16, 1024, 64, 4, 16), OK)])
+def test_shape_checks(shape, code):
+    f, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert kd.lib().kd_topk_kl_workspace_size(*shape, ctypes.byref(f), ctypes.byref(b)) == code
+
+
+def test_launch_count():
+    fl, bl = kd.kd_topk_kl_launch_count(32768, 201088, 2880, 100, 8192)
+    assert fl == 4 and bl in (1 + 4 * 3, 1 + 4 * 4)
+
+
+A = 0x10000  # fake, aligned device addresses
+
+
+def fwd(**kw):
+    a = dict(h=A, W=A, idx=A, tl=A, valid=A, T=16, V=1024, d=64, K=4, tau=1.0, chunk=16,
+             loss=A, lse=A, row_kl=None, gidx=None, ws=A, ws_bytes=1 << 40, status=A, stream=None)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return kd.lib().kd_topk_kl_forward(
+        vp(a["h"]), vp(a["W"]), vp(a["idx"]), vp(a["tl"]), vp(a["valid"]), a["T"], a["V"], a["d"],
+        a["K"], a["tau"], a["chunk"], vp(a["loss"]), vp(a["lse"]), vp(a["row_kl"]),
+        vp(a["gidx"]), vp(a["ws"]), a["ws_bytes"], vp(a["status"]), vp(a["stream"]))
+
+
+def bwd(**kw):
+    a = dict(h=A, W=A, idx=A, tl=A, valid=A, T=16, V=1024, d=64, K=4, tau=1.0, chunk=16,
+             lse=A, g=1.0, dh=A, dW=A, ws=A, ws_bytes=1 << 40, status=A, stream=None)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return kd.lib().kd_topk_kl_backward(
+        vp(a["h"]), vp(a["W"]), vp(a["idx"]), vp(a["tl"]), vp(a["valid"]), a["T"], a["V"], a["d"],
+        a["K"], a["tau"], a["chunk"], vp(a["lse"]), a["g"], vp(a["dh"]), vp(a["dW"]), vp(a["ws"]),
+        a["ws_bytes"], vp(a["status"]), vp(a["stream"]))
+
+
+@pytest.mark.parametrize("kw", [dict(h=None), dict(W=None), dict(idx=None), dict(tl=None),
+                                dict(valid=None), dict(ws=None), dict(status=None),
+                                dict(loss=None), dict(lse=None), dict(tau=0.0),
+                                dict(tau=-1.0), dict(tau=float("inf")), dict(tau=float("nan")),
+                                dict(h=A + 8), dict(W=A + 2), dict(ws=A + 4), dict(idx=A + 2),
+                                dict(T=0), dict(K=0)])
+def test_forward_invalid_args(kw):
+    assert fwd(**kw) == INVALID
+
+
+@pytest.mark.parametrize("kw", [dict(lse=None), dict(dh=None), dict(dW=None), dict(dh=A + 4),
+                                dict(g=float("nan")), dict(tau=0.0), dict(h=None)])
+def test_backward_invalid_args(kw):
+    assert bwd(**kw) == INVALID
+
+
+def test_shape_limits_reported_as_unsupported():
+    assert fwd(V=1020) == UNSUPPORTED
+    assert fwd(d=100) == UNSUPPORTED
+    assert bwd(K=2000) == UNSUPPORTED
+
+
+def test_workspace_too_small():
+    f, b = kd.kd_topk_kl_workspace_size(16, 1024, 64, 4, 16)
+    assert fwd(ws_bytes=f - 1) == WORKSPACE
+    assert bwd(ws_bytes=b - 1) == WORKSPACE
+
+
+def test_diag_and_selftest_arg_checks():
+    vp = ctypes.c_void_p
+    L = kd.lib()
+    assert L.kd_gemm_bf16_diag(None, vp(A), vp(A), 8, 8, 8, 0, 0, vp(A), None) == INVALID
+    assert L.kd_gemm_bf16_diag(vp(A), vp(A), vp(A), 8, 8, 8, 2, 0, vp(A), None) == INVALID
+    assert L.kd_gemm_bf16_diag(vp(A), vp(A), vp(A), 12, 8, 8, 0, 0, vp(A), None) == UNSUPPORTED
+    assert L.kd_pipeline_wait_selftest(0, vp(A), None) == INVALID
+    assert L.kd_pipeline_wait_selftest(2_000_000_000, vp(A), None) == INVALID
+    assert L.kd_pipeline_wait_selftest(1000, None, None) == INVALID
