@@ -140,23 +140,29 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+DEVICE_SOURCES = ("kd_kernels.cuh", "kd_ptx.cuh")
+
+
+def device_source_sha256() -> str:
+    """Hash of the device-code files the GEMM kernel is compiled from."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "chunked_top_kl_logit_b300", "csrc")
+    for name in DEVICE_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
 def load_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from a committed ncu summary, only if
-    the kernel sources still hash to what was profiled (else None)."""
-    import hashlib
+    the device code still hashes to what was profiled (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f).get(kernel)
-    if not d:
-        return None
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "chunked_top_kl_logit_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest() != d.get("csrc_sha256"):
+    if not d or d.get("device_sha256") != device_source_sha256():
         return None
     return d.get("bytes_per_launch")
 
