@@ -27,7 +27,8 @@ import torch
 
 __all__ = [
     "KD_OK", "KDError", "lib", "library_path", "status_string",
-    "kd_topk_kl_workspace_size", "kd_topk_kl_launch_count", "kd_topk_kl_forward", "kd_topk_kl_backward",
+    "kd_topk_kl_workspace_size", "kd_topk_kl_launch_count", "kd_topk_kl_forward",
+    "kd_topk_kl_forward_noalloc", "kd_topk_kl_backward",
     "kd_gemm_bf16_diag", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
 ]
 
@@ -68,6 +69,9 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_backward.restype = ctypes.c_int
         L.kd_topk_kl_status_string.argtypes = [ctypes.c_int]
         L.kd_topk_kl_status_string.restype = ctypes.c_char_p
+        L.kd_topk_kl_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, f32,
+                                                 vp, vp, vp, vp, vp, vp]
+        L.kd_topk_kl_forward_noalloc.restype = ctypes.c_int
         L.kd_gemm_bf16_diag.argtypes = [vp, vp, vp, i64, i64, i64, i32, i32, vp, vp]
         L.kd_gemm_bf16_diag.restype = ctypes.c_int
         L.kd_pipeline_wait_selftest.argtypes = [ctypes.c_uint64, vp, vp]
@@ -125,6 +129,19 @@ def kd_topk_kl_forward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, los
                                   _ptr(lse), _ptr(row_kl), _ptr(gathered_idx), _ptr(ws),
                                   ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
     _check(rc, "kd_topk_kl_forward")
+
+
+def kd_topk_kl_forward_noalloc(h, W, teacher_idx, teacher_logits, valid, tau, loss, lse,
+                               row_kl=None, gathered_idx=None, *, dev_status, stream=None):
+    """Forward on the library's built-in 32 MiB scratch (no workspace argument)."""
+    T, d = h.shape
+    V = W.shape[0]
+    K = teacher_idx.shape[1]
+    rc = lib().kd_topk_kl_forward_noalloc(_ptr(h), _ptr(W), _ptr(teacher_idx),
+                                          _ptr(teacher_logits), _ptr(valid), T, V, d, K,
+                                          float(tau), _ptr(loss), _ptr(lse), _ptr(row_kl),
+                                          _ptr(gathered_idx), _ptr(dev_status), _stream(stream))
+    _check(rc, "kd_topk_kl_forward_noalloc")
 
 
 def kd_topk_kl_backward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, lse, grad_loss,

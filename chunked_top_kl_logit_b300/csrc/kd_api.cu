@@ -220,6 +220,43 @@ void logit_schedule(GemmParams& p, int64_t rows, int64_t V, int64_t d) {
 
 }  // namespace
 
+// ------------------------------------------------------------------
+// Built-in scratch for kd_topk_kl_forward_noalloc.  Callers that cannot
+// allocate device memory get this fixed array as the forward's workspace.
+// It lives in the library's device image, so every GPU that loads the
+// library holds these bytes until the process exits.
+static constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(32) << 20;  // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+// Device address of g_noalloc_scratch on the current device.  The symbol's
+// name in host code is only a host-side stand-in, so the address is looked up
+// with cudaGetSymbolAddress once per device (with that device current) and
+// cached.
+void* noalloc_scratch_address(int* rc) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static void* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *rc = KD_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      *rc = KD_ERR_CUDA;
+      return nullptr;
+    }
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* kd_topk_kl_status_string(int status) {
@@ -231,6 +268,7 @@ const char* kd_topk_kl_status_string(int status) {
     case KD_ERR_CUDA: return "CUDA call failed";
     case KD_ERR_INDEX_RANGE: return "teacher index outside [0, V)";
     case KD_ERR_TIMEOUT: return "bounded pipeline wait timed out";
+    case KD_ERR_SCRATCH_LIMIT: return "shape needs more than the built-in 32 MiB scratch array";
     default: return "unknown status";
   }
 }
@@ -453,6 +491,25 @@ int kd_pipeline_wait_selftest(uint64_t limit_ns, int32_t* dev_status,
   if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
   kd_wait_selftest_kernel<<<1, 32, 0, st>>>(limit_ns, dev_status);
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+int kd_topk_kl_forward_noalloc(const void* h, const void* W, const int32_t* teacher_idx,
+                               const float* teacher_logits, const uint8_t* valid, int64_t T,
+                               int64_t V, int64_t d, int32_t K, float tau, float* loss, float* lse,
+                               float* row_kl, int32_t* gathered_idx, int32_t* dev_status,
+                               struct CUstream_st* stream) {
+  int rc = check_shape(T, V, d, K, 1);
+  if (rc != KD_OK) return rc;
+  if (make_layout(T, V, d, K, 1).fwd_total > kNoAllocScratchBytes) return KD_ERR_SCRATCH_LIMIT;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  void* ws = noalloc_scratch_address(&rc);
+  if (!ws) return rc;
+  // The forward resets, on `stream`, the valid-row counter and the status word
+  // it accumulates into, and overwrites every other scratch entry it reads.
+  return kd_topk_kl_forward(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, 1, loss,
+                            lse, row_kl, gathered_idx, ws, kNoAllocScratchBytes, dev_status,
+                            stream);
 }
 
 }  // extern "C"

@@ -66,7 +66,8 @@ typedef enum kd_status {
   KD_ERR_WORKSPACE = 3,    /* ws_bytes smaller than kd_topk_kl_workspace_size() */
   KD_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
   KD_ERR_INDEX_RANGE = 5,  /* device: a teacher index is outside [0, V) */
-  KD_ERR_TIMEOUT = 6       /* device: a bounded pipeline wait ran out */
+  KD_ERR_TIMEOUT = 6,      /* device: a bounded pipeline wait ran out */
+  KD_ERR_SCRATCH_LIMIT = 7 /* kd_topk_kl_forward_noalloc: shape too big for its scratch */
 } kd_status;
 
 /*
@@ -156,6 +157,36 @@ int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t
  * int32, reset to 0 first) and returns, leaving the context usable.
  */
 int kd_pipeline_wait_selftest(uint64_t limit_ns, int32_t* dev_status, struct CUstream_st* stream);
+
+/*
+ * Forward without any allocation, for callers that cannot call cudaMalloc:
+ * for example code that runs inside another framework's memory manager, which
+ * owns the whole device pool and forbids side allocations, or a host runtime
+ * that allows no device allocation after start-up (cudaMalloc can also
+ * synchronise the device, which some callers must avoid).  The pages have no
+ * counterpart to this entry point; it exists for those callers only.
+ *
+ * Same inputs, outputs and results as kd_topk_kl_forward, but the workspace
+ * is a fixed 32 MiB array built into the library (no ws / ws_bytes and no
+ * chunk argument).  Shapes whose forward workspace (kd_topk_kl_workspace_size
+ * *fwd_bytes) exceeds 32 MiB are rejected with KD_ERR_SCRATCH_LIMIT before
+ * anything is launched; at V = 201088, K = 100 that admits up to about 7300 rows.
+ * The library calls no cudaMalloc, cudaFree or other allocating routine here.
+ *
+ * - Every GPU that loads the library holds the 32 MiB array until the process
+ *   exits.
+ * - The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture.
+ * - All calls share the one array per device, and it keeps the last call's
+ *   contents.  Calls whose work overlaps on the GPU (different streams, or
+ *   several host threads) race on it; serialise them.
+ */
+int kd_topk_kl_forward_noalloc(const void* h, const void* W, const int32_t* teacher_idx,
+                               const float* teacher_logits, const uint8_t* valid, int64_t T,
+                               int64_t V, int64_t d, int32_t K, float tau, float* loss, float* lse,
+                               float* row_kl, int32_t* gathered_idx, int32_t* dev_status,
+                               struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }
