@@ -100,7 +100,7 @@ int choose_splits(int64_t tiles, int64_t k_steps) {
 struct Layout {
   size_t nvalid, losspart, sidx, sp, sslot, tterm;  // shared by both passes
   size_t zg, part;                                  // forward
-  size_t dz, dhpart;                                // backward
+  size_t rowmap, hc, dz, dhpart;                    // backward
   size_t fwd_total, bwd_total;
   int64_t rows_chunk;
   int bn_d, dh_splits;
@@ -123,6 +123,8 @@ Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
   L.bn_d = pick_bn(d);
   L.dh_splits = choose_splits(cdiv(L.rows_chunk, BM) * (d / L.bn_d), cdiv(V, BK));
   off = common;
+  L.rowmap = off;   off += al256(static_cast<size_t>(T) * 4);
+  L.hc = off;       off += al256(static_cast<size_t>(L.rows_chunk * d) * 2);
   L.dz = off;       off += al256(static_cast<size_t>(L.rows_chunk * V) * 2);
   L.dhpart = off;   off += al256(static_cast<size_t>(L.dh_splits - 1) * L.rows_chunk * d * 4);
   L.bwd_total = off;
@@ -290,8 +292,10 @@ int kd_topk_kl_launch_count(int64_t T, int64_t V, int64_t d, int32_t K, int64_t 
   const Layout L = make_layout(T, V, d, K, chunk);
   const int64_t chunks = cdiv(T, L.rows_chunk);
   if (fwd_launches) *fwd_launches = 4;  // prep, logit GEMM, combine, loss
+  // prep + row compaction, then per chunk: row gather, recompute, dh, [dh split
+  // reduce], dW
   if (bwd_launches)
-    *bwd_launches = static_cast<int32_t>(1 + chunks * (L.dh_splits > 1 ? 4 : 3));
+    *bwd_launches = static_cast<int32_t>(2 + chunks * (L.dh_splits > 1 ? 5 : 4));
   return KD_OK;
 }
 
@@ -362,27 +366,40 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const Ws w = carve(ws, L);
   char* wb = static_cast<char*>(ws);
+  int* rowmap = reinterpret_cast<int*>(wb + L.rowmap);
+  __nv_bfloat16* hc = reinterpret_cast<__nv_bfloat16*>(wb + L.hc);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(wb + L.dz);
   float* dhpart = reinterpret_cast<float*>(wb + L.dhpart);
   const float inv_tau = 1.0f / tau;
   const int BN = L.bn_d;
   const int S = L.dh_splits;
-  const __nv_bfloat16* hb = static_cast<const __nv_bfloat16*>(h);
+  const int64_t C = L.rows_chunk;
 
+  // Rows with valid = 0 have an exactly zero gradient: dh starts at zero and
+  // the chunks below run over the valid rows only, compacted in ascending
+  // order.  Their count stays on the device; every kernel clamps to it.
+  if (cudaMemsetAsync(dh, 0, static_cast<size_t>(T * d) * sizeof(float), st) != cudaSuccess)
+    return KD_ERR_CUDA;
   if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, inv_tau, w, dev_status, st)))
     return rc;
+  kd_compact_rows_kernel<<<1, 1024, 0, st>>>(valid, static_cast<int>(T), rowmap);
+  if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
 
-  for (int64_t c0 = 0; c0 < T; c0 += L.rows_chunk) {
-    const int64_t rows = (T - c0) < L.rows_chunk ? (T - c0) : L.rows_chunk;
-    const __nv_bfloat16* hc = hb + c0 * d;
+  for (int64_t c0 = 0; c0 < T; c0 += C) {
     CUtensorMap ta, tb;
+    const int gblocks = sms * 4;
+
+    // (0) the chunk's valid rows of h, zero-padded to C rows
+    kd_gather_rows_kernel<<<gblocks, 256, 0, st>>>(
+        static_cast<const uint4*>(h), rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
+        static_cast<int>(d / 8), reinterpret_cast<uint4*>(hc));
+    if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
 
     // (1) recompute the chunk's logit tiles and write G as bf16
-    if (!make_map(&ta, hc, d, rows, d, BM) || !make_map(&tb, W, d, V, d, ZBN)) return KD_ERR_CUDA;
+    if (!make_map(&ta, hc, d, C, d, BM) || !make_map(&tb, W, d, V, d, ZBN)) return KD_ERR_CUDA;
     GemmParams p = base_params(0, 0, ZBN);
-    logit_schedule(p, rows, V, d);
+    logit_schedule(p, C, V, d);
     p.status = dev_status;
-    p.row0 = static_cast<int>(c0);
     p.K = K;
     p.sidx = w.sidx;
     p.sp = w.sp;
@@ -395,12 +412,18 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     p.grad_loss = grad_loss;
     p.dz = dz;
     p.dz_ld = V;
+    p.dyn_count = w.nvalid;
+    p.dyn_base = static_cast<int>(c0);
+    p.dyn_cap = static_cast<int>(C);
+    p.dyn_kind = 1;
+    p.rowmap = rowmap;
+    p.rowmap_base = static_cast<int>(c0);
     if ((rc = launch_gemm<EPI_DZ>(ta, tb, p, sms, st))) return rc;
 
     // (2) dh rows of the chunk = G W, contraction over V split S ways
-    if (!make_map(&ta, dz, V, rows, V, BM) || !make_map(&tb, W, d, V, d, 64)) return KD_ERR_CUDA;
+    if (!make_map(&ta, dz, V, C, V, BM) || !make_map(&tb, W, d, V, d, 64)) return KD_ERR_CUDA;
     GemmParams q = base_params(0, 1, BN);
-    q.m_tiles = static_cast<int>(cdiv(rows, BM));
+    q.m_tiles = static_cast<int>(cdiv(C, BM));
     q.n_tiles = static_cast<int>(d / BN);
     q.splits = S;
     q.num_tiles = q.m_tiles * q.n_tiles * S;
@@ -408,29 +431,35 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     q.ks_per_split = static_cast<int>(cdiv(q.k_steps, S));
     q.n_fast = 1;
     q.group_m = 1;
-    q.M = static_cast<int>(rows);
+    q.M = static_cast<int>(C);
     q.N = static_cast<int>(d);
     q.status = dev_status;
-    q.out = dh + c0 * d;
+    q.out = dh;
     q.out2 = dhpart;
     q.ld_out = d;
-    q.split_stride = rows * d;
+    q.split_stride = C * d;
     q.accumulate = 0;
+    q.dyn_count = w.nvalid;
+    q.dyn_base = static_cast<int>(c0);
+    q.dyn_cap = static_cast<int>(C);
+    q.dyn_kind = 1;
+    q.rowmap = rowmap;
+    q.rowmap_base = static_cast<int>(c0);
     if ((rc = launch_gemm<EPI_STORE>(ta, tb, q, sms, st))) return rc;
     if (S > 1) {
-      const int64_t n4 = rows * d / 4;
-      const unsigned blocks = static_cast<unsigned>(sms) * 4;
-      kd_split_reduce_kernel<<<blocks, 256, 0, st>>>(dh + c0 * d, dhpart, S - 1, n4, rows * d);
+      kd_split_reduce_rows_kernel<<<gblocks, 256, 0, st>>>(
+          dh, dhpart, S - 1, rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
+          static_cast<int>(d / 4), C * d);
       if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
     }
 
-    // (3) dW (+)= G^T h_c, contraction over the chunk's rows
-    if (!make_map(&ta, dz, V, rows, V, 64) || !make_map(&tb, hc, d, rows, d, 64)) return KD_ERR_CUDA;
+    // (3) dW (+)= G^T h_c, contraction over the chunk's valid rows
+    if (!make_map(&ta, dz, V, C, V, 64) || !make_map(&tb, hc, d, C, d, 64)) return KD_ERR_CUDA;
     GemmParams r = base_params(1, 1, BN);
     r.m_tiles = static_cast<int>(cdiv(V, BM));
     r.n_tiles = static_cast<int>(d / BN);
     r.num_tiles = r.m_tiles * r.n_tiles;
-    r.k_steps = static_cast<int>(cdiv(rows, BK));
+    r.k_steps = static_cast<int>(cdiv(C, BK));
     r.ks_per_split = r.k_steps;
     r.n_fast = 1;
     r.group_m = 1;
@@ -441,6 +470,10 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     r.out2 = nullptr;
     r.ld_out = d;
     r.accumulate = c0 > 0 ? 1 : 0;
+    r.dyn_count = w.nvalid;
+    r.dyn_base = static_cast<int>(c0);
+    r.dyn_cap = static_cast<int>(C);
+    r.dyn_kind = 2;
     if ((rc = launch_gemm<EPI_STORE>(ta, tb, r, sms, st))) return rc;
   }
   return KD_OK;

@@ -77,14 +77,43 @@ struct GemmParams {
   float grad_loss;
   __nv_bfloat16* dz;      // [rows][dz_ld] chunk buffer
   int64_t dz_ld;
+  // Row counts known only on the device (the backward works on the valid rows
+  // only): rows = clamp(*dyn_count - dyn_base, 0, dyn_cap).  dyn_kind 0: static
+  // shape; 1: rows are the M dimension; 2: rows are the contraction (splits == 1).
+  const int* dyn_count;
+  int dyn_base, dyn_cap, dyn_kind;
+  // Compact row -> original row, rowmap[rowmap_base + local row]; null = identity.
+  const int* rowmap;
+  int rowmap_base;
 };
+
+// Per-launch schedule, resolved on the device at kernel start.
+struct Sched {
+  int m_tiles, num_tiles, k_steps, ks_per_split, M;
+};
+
+__device__ __forceinline__ Sched make_sched(const GemmParams& p) {
+  Sched s{p.m_tiles, p.num_tiles, p.k_steps, p.ks_per_split, p.M};
+  if (p.dyn_kind != 0) {
+    const int rows = max(0, min(*p.dyn_count - p.dyn_base, p.dyn_cap));
+    if (p.dyn_kind == 1) {
+      s.M = rows;
+      s.m_tiles = (rows + BM - 1) / BM;
+      s.num_tiles = s.m_tiles * p.n_tiles * p.splits;
+    } else {
+      s.k_steps = (rows + BK - 1) / BK;
+      s.ks_per_split = s.k_steps;
+    }
+  }
+  return s;
+}
 
 struct TileCoord {
   int m, n, s;
 };
 
-__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
-  const int per_split = p.m_tiles * p.n_tiles;
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, const Sched& sc, int t) {
+  const int per_split = sc.m_tiles * p.n_tiles;
   TileCoord c;
   c.s = t / per_split;
   const int r = t - c.s * per_split;
@@ -95,7 +124,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
     const int gsz = p.group_m * p.n_tiles;
     const int g = r / gsz;
     const int m0 = g * p.group_m;
-    const int gm = min(p.group_m, p.m_tiles - m0);
+    const int gm = min(p.group_m, sc.m_tiles - m0);
     const int j = r - g * gsz;
     c.n = j / gm;
     c.m = m0 + (j - c.n * gm);
@@ -115,7 +144,8 @@ __device__ __forceinline__ int lower_bound_row(const int* __restrict__ s, int K,
 
 // ------------------------------------------------------------------ roles
 
-__device__ __forceinline__ void producer_role(const GemmParams& p, const CUtensorMap* tmA,
+__device__ __forceinline__ void producer_role(const GemmParams& p, const Sched& sc,
+                                              const CUtensorMap* tmA,
                                               const CUtensorMap* tmB, uint8_t* smem,
                                               uint64_t* full, uint64_t* empty,
                                               volatile int* abort_flag) {
@@ -125,10 +155,10 @@ __device__ __forceinline__ void producer_role(const GemmParams& p, const CUtenso
   uint32_t phase = 0;
   int issued = 0;
   bool ok = true;
-  for (int t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-    const TileCoord c = decode_tile(p, t);
-    const int kb = c.s * p.ks_per_split;
-    const int ke = min(p.k_steps, kb + p.ks_per_split);
+  for (int t = blockIdx.x; t < sc.num_tiles && ok; t += gridDim.x) {
+    const TileCoord c = decode_tile(p, sc, t);
+    const int kb = c.s * sc.ks_per_split;
+    const int ke = min(sc.k_steps, kb + sc.ks_per_split);
     for (int ks = kb; ks < ke; ++ks) {
       if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
       uint8_t* sa = smem + static_cast<size_t>(stage) * p.stage_bytes;
@@ -158,7 +188,8 @@ __device__ __forceinline__ void producer_role(const GemmParams& p, const CUtenso
   }
 }
 
-__device__ __forceinline__ void mma_role(const GemmParams& p, uint8_t* smem, uint64_t* full,
+__device__ __forceinline__ void mma_role(const GemmParams& p, const Sched& sc, uint8_t* smem,
+                                         uint64_t* full,
                                          uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
                                          uint64_t* drain, uint32_t tmem_base,
                                          volatile int* abort_flag) {
@@ -171,14 +202,18 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, uint8_t* smem, uin
   uint32_t phase = 0;
   bool ok = true;
   int lt = 0;
-  for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
-    const TileCoord c = decode_tile(p, t);
-    const int kb = c.s * p.ks_per_split;
-    const int ke = min(p.k_steps, kb + p.ks_per_split);
+  for (int t = blockIdx.x; t < sc.num_tiles; t += gridDim.x, ++lt) {
+    const TileCoord c = decode_tile(p, sc, t);
+    const int kb = c.s * sc.ks_per_split;
+    const int ke = min(sc.k_steps, kb + sc.ks_per_split);
     const int acc = lt & 1;
     const uint32_t use = static_cast<uint32_t>(lt >> 1);
     if (!mbar_wait(&tempty[acc], (use & 1u) ^ 1u, abort_flag, p.status)) { ok = false; break; }
     tc_fence_after();
+    if (kb >= ke) {          // empty contraction: the epilogue writes zeros, no MMA
+      mbar_arrive(&tfull[acc]);
+      continue;
+    }
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * 256);
     for (int ks = kb; ks < ke; ++ks) {
       if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
@@ -207,12 +242,13 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, uint8_t* smem, uin
 
 // Forward: per (row, vocab tile) natural-log lse partial of z/tau and the
 // gather of z/tau at the row's cached indices that fall inside the tile.
-__device__ __forceinline__ void epi_fwd(const GemmParams& p, const TileCoord& c, int acc,
+__device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, const TileCoord& c,
+                                        int acc,
                                         uint32_t tmem_row, int r_in_tile, uint64_t* tfull,
                                         uint64_t* tempty, uint32_t use, volatile int* abort_flag,
                                         bool& ok) {
   const int lrow = c.m * BM + r_in_tile;
-  const bool row_ok = lrow < p.M;
+  const bool row_ok = lrow < sc_.M;
   const int64_t grow = static_cast<int64_t>(p.row0) + lrow;
   const int v0 = c.n * ZBN;
   const int* srow = p.sidx + grow * p.K;
@@ -268,20 +304,23 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const TileCoord& c,
 }
 
 // Backward: G = s_t (exp(z/tau - lse) - scatter p) / tau as bf16 into the chunk buffer.
-__device__ __forceinline__ void epi_dz(const GemmParams& p, const TileCoord& c, int acc,
+__device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, const TileCoord& c,
+                                       int acc,
                                        uint32_t tmem_row, int r_in_tile, uint64_t* tfull,
                                        uint64_t* tempty, uint32_t use, volatile int* abort_flag,
                                        bool& ok) {
   const int lrow = c.m * BM + r_in_tile;
-  const bool row_ok = lrow < p.M;
-  const int64_t grow = static_cast<int64_t>(p.row0) + lrow;
+  const bool row_ok = lrow < p.M;      // inside the chunk buffer: always stored
+  const bool active = lrow < sc_.M;    // a real row of this chunk
+  int64_t grow = 0;
+  if (active) grow = p.rowmap ? p.rowmap[p.rowmap_base + lrow] : static_cast<int64_t>(p.row0) + lrow;
   const int v0 = c.n * ZBN;
   const int* srow = p.sidx + grow * p.K;
   float sc = 0.f;   // g * valid / N_valid / tau
   float lb = 0.f;   // lse in base 2
   int pos = p.K;
   int nxt = INT_MAX;
-  if (row_ok) {
+  if (active) {
     const int nv = *p.nvalid;
     if (p.valid[grow] && nv > 0) {
       sc = p.grad_loss / static_cast<float>(nv) * p.inv_tau;
@@ -344,16 +383,21 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const TileCoord& c, 
 }
 
 // fp32 tile store, optionally accumulating into the existing output.
-__device__ __forceinline__ void epi_store(const GemmParams& p, const TileCoord& c, int acc,
+__device__ __forceinline__ void epi_store(const GemmParams& p, const Sched& sc_, const TileCoord& c,
+                                          int acc,
                                           uint32_t tmem_row, int r_in_tile, uint64_t* tfull,
                                           uint64_t* tempty, uint32_t use,
                                           volatile int* abort_flag, bool& ok) {
   const int row = c.m * BM + r_in_tile;
-  const bool row_ok = row < p.M;
+  const bool row_ok = row < sc_.M;
   const int n0 = c.n * p.BN;
+  int64_t orow_idx = row;
+  if (row_ok && p.rowmap && c.s == 0) orow_idx = p.rowmap[p.rowmap_base + row];
   float* orow = (c.s == 0 ? p.out : p.out2 + static_cast<int64_t>(c.s - 1) * p.split_stride) +
-                static_cast<int64_t>(row) * p.ld_out;
+                orow_idx * p.ld_out;
   const bool accum = p.accumulate && c.s == 0;
+  const int kb = c.s * sc_.ks_per_split;
+  const bool kempty = kb >= min(sc_.k_steps, kb + sc_.ks_per_split);
   bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
   ok = __all_sync(0xffffffffu, w);
   if (!ok) return;
@@ -363,8 +407,14 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const TileCoord& 
     const int cb = n0 + cc * 32;
     if (cb >= p.N) break;
     uint32_t r[32];
-    tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
-    tmem_ld_wait(r);
+    if (kempty) {            // nothing accumulated: the tile is zero
+      if (accum) break;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = 0u;
+    } else {
+      tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
+      tmem_ld_wait(r);
+    }
     if (row_ok) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -427,26 +477,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  const Sched sc = make_sched(p);
   if (warp == 0) {
-    if (lane == 0) producer_role(p, &tmA, &tmB, smem, full, empty, abort_flag);
+    if (lane == 0) producer_role(p, sc, &tmA, &tmB, smem, full, empty, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) mma_role(p, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
+    if (lane == 0) mma_role(p, sc, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r_in_tile = q * 32 + lane;
     const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     bool ok = true;
     int lt = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++lt) {
-      const TileCoord c = decode_tile(p, t);
+    for (int t = blockIdx.x; t < sc.num_tiles; t += gridDim.x, ++lt) {
+      const TileCoord c = decode_tile(p, sc, t);
       const int acc = lt & 1;
       const uint32_t use = static_cast<uint32_t>(lt >> 1);
       if (MODE == EPI_FWD)
-        epi_fwd(p, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+        epi_fwd(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else if (MODE == EPI_DZ)
-        epi_dz(p, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+        epi_dz(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else
-        epi_store(p, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+        epi_store(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       if (!ok) break;
     }
   }
@@ -586,17 +637,82 @@ __global__ void kd_loss_final_kernel(const double* __restrict__ losspart, int nb
   }
 }
 
-// dh[i] += sum_{s} part[s][i] in a fixed order (split-K completion).
-__global__ void kd_split_reduce_kernel(float* __restrict__ out, const float* __restrict__ part,
-                                       int nparts, int64_t n4, int64_t stride) {
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+// Valid rows in ascending order: rowmap[i] = the i-th row with valid != 0.
+// One block; fixed order, so the compaction is deterministic.
+__global__ void kd_compact_rows_kernel(const uint8_t* __restrict__ valid, int T,
+                                       int* __restrict__ rowmap) {
+  __shared__ int warp_incl[32];
+  __shared__ int base;
+  const int lane = threadIdx.x & 31;
+  const int w = threadIdx.x >> 5;
+  const int nw = blockDim.x >> 5;
+  if (threadIdx.x == 0) base = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < T; t0 += blockDim.x) {
+    const int t = t0 + threadIdx.x;
+    const int f = (t < T && valid[t]) ? 1 : 0;
+    int x = f;  // inclusive scan inside the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_incl[w] = x;
+    __syncthreads();
+    if (w == 0) {
+      int v = lane < nw ? warp_incl[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      if (lane < nw) warp_incl[lane] = v;
+    }
+    __syncthreads();
+    const int excl = base + (w > 0 ? warp_incl[w - 1] : 0) + x - f;
+    if (f) rowmap[excl] = t;
+    __syncthreads();
+    if (threadIdx.x == 0) base += warp_incl[nw - 1];
+    __syncthreads();
+  }
+}
+
+// Chunk of compacted rows: hc[i] = h[rowmap[c0 + i]] for i < rows and 0 for
+// rows <= i < cap, with rows = clamp(*nvalid - c0, 0, cap).  d8 = d / 8.
+__global__ void kd_gather_rows_kernel(const uint4* __restrict__ h, const int* __restrict__ rowmap,
+                                      const int* __restrict__ nvalid, int c0, int cap, int d8,
+                                      uint4* __restrict__ hc) {
+  const int rows = max(0, min(*nvalid - c0, cap));
+  const int64_t n = static_cast<int64_t>(cap) * d8;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    float4 a = reinterpret_cast<float4*>(out)[i];
+    const int r = static_cast<int>(i / d8);
+    const int j = static_cast<int>(i - static_cast<int64_t>(r) * d8);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < rows) v = h[static_cast<int64_t>(rowmap[c0 + r]) * d8 + j];
+    hc[i] = v;
+  }
+}
+
+// Split-K completion for dh rows of a chunk: dh[rowmap[c0 + r]] += sum_s part[s][r]
+// in a fixed order, for the chunk's rows r < clamp(*nvalid - c0, 0, cap).  d4 = d / 4.
+__global__ void kd_split_reduce_rows_kernel(float* __restrict__ dh, const float* __restrict__ part,
+                                            int nparts, const int* __restrict__ rowmap,
+                                            const int* __restrict__ nvalid, int c0, int cap,
+                                            int d4, int64_t stride) {
+  const int rows = max(0, min(*nvalid - c0, cap));
+  const int64_t n = static_cast<int64_t>(rows) * d4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int r = static_cast<int>(i / d4);
+    const int j = static_cast<int>(i - static_cast<int64_t>(r) * d4);
+    float4* dst = reinterpret_cast<float4*>(dh) + static_cast<int64_t>(rowmap[c0 + r]) * d4 + j;
+    float4 a = *dst;
     for (int s = 0; s < nparts; ++s) {
       const float4 b = reinterpret_cast<const float4*>(part + s * stride)[i];
       a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
     }
-    reinterpret_cast<float4*>(out)[i] = a;
+    *dst = a;
   }
 }
 

@@ -121,6 +121,21 @@ def test_no_valid_rows():
     assert np.abs(gpu["lse"] - ref["lse"]).max() <= LSE_ATOL
 
 
+def test_heavy_masking_leaves_empty_chunks():
+    """70% of rows masked and small chunks: the backward runs over the valid
+    rows only, so the last chunks hold no row at all (their kernels find no
+    work on the device and dW keeps the earlier chunks' sum)."""
+    x = make_inputs(workload("small_4k", T=600, d=128, V=2000, K=24, tau=1.0, idx_kind="uniform"))
+    g = torch.Generator().manual_seed(11)
+    x["valid"] = (torch.rand(600, generator=g) < 0.3).to(torch.uint8)
+    gpu = run_gpu(x, 96)
+    ref = oracle_all(x)
+    assert_forward_parity(gpu, ref)
+    assert rel_l2(gpu["dh"], ref["dh"]) <= GRAD_RL2
+    assert rel_l2(gpu["dW"], ref["dW"]) <= GRAD_RL2
+    assert np.all(gpu["dh"][x["valid"].numpy() == 0] == 0.0)
+
+
 def test_single_row_and_k1():
     x = make_inputs(workload("small_4k", T=1, d=64, V=8, K=1, idx_kind="uniform", mask_kind="all"))
     gpu = run_gpu(x, 1)
