@@ -503,8 +503,10 @@ int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t
   p.num_tiles = p.m_tiles * p.n_tiles;
   p.k_steps = static_cast<int>(cdiv(Kd, BK));
   p.ks_per_split = p.k_steps;
-  p.n_fast = 1;
-  p.group_m = 1;
+  // the shorter tile dimension runs fastest, so that the CTAs running
+  // together share the operand slabs of the longer one
+  p.n_fast = p.n_tiles <= p.m_tiles ? 1 : 0;
+  p.group_m = p.m_tiles;
   p.M = static_cast<int>(M);
   p.N = static_cast<int>(N);
   p.status = dev_status;
