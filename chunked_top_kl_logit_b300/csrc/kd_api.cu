@@ -72,38 +72,26 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-int pick_bn(int64_t d) {
-  if (d % 256 == 0) return 256;
-  if (d % 192 == 0) return 192;
-  if (d % 128 == 0) return 128;
-  return 64;
-}
+// Largest split count the dh contraction may use (the device picks the actual
+// count from the chunk's row count; each split keeps at least 32 k-steps).
+constexpr int kMaxDhSplits = 4;
+constexpr int kGradBN = 256;  // gradient contractions: 128 hidden units x 256 rows per tile
 
-// Split count over the vocabulary for dh = G W: enough (tile, split) units to
-// keep the wave-quantisation loss small, each split at least 32 k-steps long.
-int choose_splits(int64_t tiles, int64_t k_steps) {
-  int best = 1;
-  double best_eff = 0.0;
-  for (int s = 1; s <= 8; ++s) {
-    if (s > 1 && k_steps / s < 32) break;
-    const double units = static_cast<double>(tiles) * s;
-    const double eff = units / (std::ceil(units / kPolicySMs) * kPolicySMs);
-    if (eff > best_eff + 1e-9) {
-      best_eff = eff;
-      best = s;
-    }
-    if (eff >= 0.95) break;
-  }
-  return best;
+int dh_max_splits(int64_t V) {
+  const int64_t ks = cdiv(V, BK);
+  int s = 1;
+  while (s < kMaxDhSplits && ks / (s + 1) >= 32) ++s;
+  return s;
 }
 
 struct Layout {
   size_t nvalid, losspart, sidx, sp, sslot, tterm;  // shared by both passes
   size_t zg, part;                                  // forward
-  size_t rowmap, hc, dz, dhpart;                    // backward
+  size_t rowmap, split_info, hc, dz, dhpart;        // backward
   size_t fwd_total, bwd_total;
   int64_t rows_chunk;
-  int bn_d, dh_splits;
+  int dh_splits;      // largest split count of the dh contraction
+  int64_t part_rows;  // rows of dh partials the split blocks may use
 };
 
 Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
@@ -120,13 +108,14 @@ Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
   L.part = off;     off += al256(static_cast<size_t>(cdiv(V, ZBN) * T) * 4);
   L.fwd_total = off;
   L.rows_chunk = chunk < T ? chunk : T;
-  L.bn_d = pick_bn(d);
-  L.dh_splits = choose_splits(cdiv(L.rows_chunk, BM) * (d / L.bn_d), cdiv(V, BK));
+  L.dh_splits = dh_max_splits(V);
+  L.part_rows = L.dh_splits > 1 ? 2 * cdiv(L.rows_chunk, kGradBN) * kGradBN : 0;
   off = common;
-  L.rowmap = off;   off += al256(static_cast<size_t>(T) * 4);
-  L.hc = off;       off += al256(static_cast<size_t>(L.rows_chunk * d) * 2);
-  L.dz = off;       off += al256(static_cast<size_t>(L.rows_chunk * V) * 2);
-  L.dhpart = off;   off += al256(static_cast<size_t>(L.dh_splits - 1) * L.rows_chunk * d * 4);
+  L.rowmap = off;     off += al256(static_cast<size_t>(T) * 4);
+  L.split_info = off; off += 256;
+  L.hc = off;         off += al256(static_cast<size_t>(L.rows_chunk * d) * 2);
+  L.dz = off;         off += al256(static_cast<size_t>(L.rows_chunk * V) * 2);
+  L.dhpart = off;     off += al256(static_cast<size_t>(L.part_rows * d) * 4);
   L.bwd_total = off;
   return L;
 }
@@ -370,8 +359,8 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
   __nv_bfloat16* hc = reinterpret_cast<__nv_bfloat16*>(wb + L.hc);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(wb + L.dz);
   float* dhpart = reinterpret_cast<float*>(wb + L.dhpart);
+  int* split_info = reinterpret_cast<int*>(wb + L.split_info);
   const float inv_tau = 1.0f / tau;
-  const int BN = L.bn_d;
   const int S = L.dh_splits;
   const int64_t C = L.rows_chunk;
 
@@ -420,51 +409,58 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     p.rowmap_base = static_cast<int>(c0);
     if ((rc = launch_gemm<EPI_DZ>(ta, tb, p, sms, st))) return rc;
 
-    // (2) dh rows of the chunk = G W, contraction over V split S ways
-    if (!make_map(&ta, dz, V, C, V, BM) || !make_map(&tb, W, d, V, d, 64)) return KD_ERR_CUDA;
-    GemmParams q = base_params(0, 1, BN);
-    q.m_tiles = static_cast<int>(cdiv(C, BM));
-    q.n_tiles = static_cast<int>(d / BN);
+    // (2) dh rows of the chunk, computed transposed: dh_c^T = W^T G_c^T, so a
+    // tile is 128 hidden units x 256 chunk rows (A = W as an MN-major operand,
+    // B = G K-major).  The contraction over V is split on the device when the
+    // chunk holds too few rows to fill the GPU.
+    if (!make_map(&ta, W, d, V, d, 64) || !make_map(&tb, dz, V, C, V, kGradBN))
+      return KD_ERR_CUDA;
+    GemmParams q = base_params(1, 0, kGradBN);
+    q.m_tiles = static_cast<int>(cdiv(d, BM));
+    q.n_tiles = static_cast<int>(cdiv(C, kGradBN));
     q.splits = S;
-    q.num_tiles = q.m_tiles * q.n_tiles * S;
+    q.num_tiles = q.m_tiles * q.n_tiles * S;  // upper bound; the device decides
     q.k_steps = static_cast<int>(cdiv(V, BK));
-    q.ks_per_split = static_cast<int>(cdiv(q.k_steps, S));
-    q.n_fast = 1;
-    q.group_m = 1;
-    q.M = static_cast<int>(C);
-    q.N = static_cast<int>(d);
+    q.ks_per_split = q.k_steps;
+    q.n_fast = 0;
+    q.group_m = q.m_tiles;                    // hidden-unit tiles fastest: W slabs shared
+    q.M = static_cast<int>(d);
+    q.N = static_cast<int>(C);
     q.status = dev_status;
     q.out = dh;
     q.out2 = dhpart;
     q.ld_out = d;
-    q.split_stride = C * d;
-    q.accumulate = 0;
     q.dyn_count = w.nvalid;
     q.dyn_base = static_cast<int>(c0);
     q.dyn_cap = static_cast<int>(C);
-    q.dyn_kind = 1;
+    q.dyn_kind = 3;
     q.rowmap = rowmap;
     q.rowmap_base = static_cast<int>(c0);
-    if ((rc = launch_gemm<EPI_STORE>(ta, tb, q, sms, st))) return rc;
+    q.part_rows = static_cast<int>(L.part_rows);
+    q.policy_sms = kPolicySMs;
+    q.split_info = split_info;
+    if ((rc = launch_gemm<EPI_DH>(ta, tb, q, sms, st))) return rc;
     if (S > 1) {
       kd_split_reduce_rows_kernel<<<gblocks, 256, 0, st>>>(
-          dh, dhpart, S - 1, rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
-          static_cast<int>(d / 4), C * d);
+          dh, dhpart, split_info, rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
+          static_cast<int>(d / 4));
       if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
     }
 
-    // (3) dW (+)= G^T h_c, contraction over the chunk's valid rows
-    if (!make_map(&ta, dz, V, C, V, 64) || !make_map(&tb, hc, d, C, d, 64)) return KD_ERR_CUDA;
-    GemmParams r = base_params(1, 1, BN);
-    r.m_tiles = static_cast<int>(cdiv(V, BM));
-    r.n_tiles = static_cast<int>(d / BN);
+    // (3) dW (+)= G_c^T h_c, computed transposed: dW^T = h_c^T G_c with tiles of
+    // 128 hidden units x 256 vocabulary rows (both operands MN-major), the
+    // contraction running over the chunk's valid rows.
+    if (!make_map(&ta, hc, d, C, d, 64) || !make_map(&tb, dz, V, C, V, 64)) return KD_ERR_CUDA;
+    GemmParams r = base_params(1, 1, kGradBN);
+    r.m_tiles = static_cast<int>(cdiv(d, BM));
+    r.n_tiles = static_cast<int>(cdiv(V, kGradBN));
     r.num_tiles = r.m_tiles * r.n_tiles;
     r.k_steps = static_cast<int>(cdiv(C, BK));
     r.ks_per_split = r.k_steps;
-    r.n_fast = 1;
-    r.group_m = 1;
-    r.M = static_cast<int>(V);
-    r.N = static_cast<int>(d);
+    r.n_fast = 0;
+    r.group_m = r.m_tiles;                    // hidden-unit tiles fastest: G slabs shared
+    r.M = static_cast<int>(d);
+    r.N = static_cast<int>(V);
     r.status = dev_status;
     r.out = dW;
     r.out2 = nullptr;
@@ -474,7 +470,7 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     r.dyn_base = static_cast<int>(c0);
     r.dyn_cap = static_cast<int>(C);
     r.dyn_kind = 2;
-    if ((rc = launch_gemm<EPI_STORE>(ta, tb, r, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_DW>(ta, tb, r, sms, st))) return rc;
   }
   return KD_OK;
 }

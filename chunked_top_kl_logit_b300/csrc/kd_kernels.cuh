@@ -35,7 +35,12 @@ constexpr int MAX_STAGES = 8;
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
-enum EpiMode { EPI_FWD = 0, EPI_DZ = 1, EPI_STORE = 2 };
+// EPI_STORE: plain fp32 tile store (diagnostic GEMM).  EPI_DH / EPI_DW: the
+// two gradient contractions, computed transposed (output rows = hidden units,
+// so the stores run along d and coalesce) and written through the row map /
+// accumulated; they differ only in schedule, and are separate instantiations
+// so that profiles tell them apart.
+enum EpiMode { EPI_FWD = 0, EPI_DZ = 1, EPI_STORE = 2, EPI_DH = 3, EPI_DW = 4 };
 
 struct GemmParams {
   // schedule: tile t -> (split s, m tile, n tile)
@@ -79,30 +84,73 @@ struct GemmParams {
   int64_t dz_ld;
   // Row counts known only on the device (the backward works on the valid rows
   // only): rows = clamp(*dyn_count - dyn_base, 0, dyn_cap).  dyn_kind 0: static
-  // shape; 1: rows are the M dimension; 2: rows are the contraction (splits == 1).
+  // shape; 1: rows are the M dimension; 2: rows are the contraction (splits == 1);
+  // 3: rows are the N dimension.
   const int* dyn_count;
   int dyn_base, dyn_cap, dyn_kind;
   // Compact row -> original row, rowmap[rowmap_base + local row]; null = identity.
   const int* rowmap;
   int rowmap_base;
+  // Split count chosen on the device (dyn_kind 3 with splits > 1): at most
+  // `splits`, limited so that (S - 1) partial blocks of n_tiles*BN rows fit in
+  // part_rows rows, scored for policy_sms CTAs.  CTA 0 publishes
+  // {S, n_tiles*BN} in split_info for the reduction that follows.
+  int part_rows, policy_sms;
+  int* split_info;
 };
 
 // Per-launch schedule, resolved on the device at kernel start.
 struct Sched {
-  int m_tiles, num_tiles, k_steps, ks_per_split, M;
+  int m_tiles, n_tiles, num_tiles, k_steps, ks_per_split, splits, M, N;
 };
 
+// Split count for `tiles` output tiles over `k_steps` contraction steps: the
+// fewest splits whose (tile, split) units fill the policy's CTA count to 95%,
+// else the best fill; each split keeps at least 32 steps.
+__host__ __device__ inline int pick_splits(int tiles, int k_steps, int max_splits, int sms) {
+  if (tiles <= 0 || sms <= 0) return 1;
+  int best = 1;
+  double best_eff = 0.0;
+  for (int s = 1; s <= max_splits; ++s) {
+    if (s > 1 && k_steps / s < 32) break;
+    const long long units = static_cast<long long>(tiles) * s;
+    const long long waves = (units + sms - 1) / sms;
+    const double eff = static_cast<double>(units) / static_cast<double>(waves * sms);
+    if (eff > best_eff + 1e-9) {
+      best_eff = eff;
+      best = s;
+    }
+    if (eff >= 0.95) break;
+  }
+  return best;
+}
+
 __device__ __forceinline__ Sched make_sched(const GemmParams& p) {
-  Sched s{p.m_tiles, p.num_tiles, p.k_steps, p.ks_per_split, p.M};
+  Sched s{p.m_tiles, p.n_tiles, p.num_tiles, p.k_steps, p.ks_per_split, p.splits, p.M, p.N};
   if (p.dyn_kind != 0) {
     const int rows = max(0, min(*p.dyn_count - p.dyn_base, p.dyn_cap));
     if (p.dyn_kind == 1) {
       s.M = rows;
       s.m_tiles = (rows + BM - 1) / BM;
-      s.num_tiles = s.m_tiles * p.n_tiles * p.splits;
-    } else {
+      s.num_tiles = s.m_tiles * s.n_tiles * s.splits;
+    } else if (p.dyn_kind == 2) {
       s.k_steps = (rows + BK - 1) / BK;
       s.ks_per_split = s.k_steps;
+    } else {
+      s.N = rows;
+      s.n_tiles = (rows + p.BN - 1) / p.BN;
+      if (p.splits > 1) {
+        const int pad = s.n_tiles * p.BN;
+        int smax = p.splits;
+        if (pad > 0) smax = min(smax, 1 + p.part_rows / pad);
+        s.splits = pick_splits(s.m_tiles * s.n_tiles, s.k_steps, smax, p.policy_sms);
+        s.ks_per_split = (s.k_steps + s.splits - 1) / s.splits;
+        if (p.split_info && blockIdx.x == 0 && threadIdx.x == 0) {
+          p.split_info[0] = s.splits;
+          p.split_info[1] = pad;
+        }
+      }
+      s.num_tiles = s.m_tiles * s.n_tiles * s.splits;
     }
   }
   return s;
@@ -113,15 +161,15 @@ struct TileCoord {
 };
 
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, const Sched& sc, int t) {
-  const int per_split = sc.m_tiles * p.n_tiles;
+  const int per_split = sc.m_tiles * sc.n_tiles;
   TileCoord c;
   c.s = t / per_split;
   const int r = t - c.s * per_split;
   if (p.n_fast) {
-    c.m = r / p.n_tiles;
-    c.n = r - c.m * p.n_tiles;
+    c.m = r / sc.n_tiles;
+    c.n = r - c.m * sc.n_tiles;
   } else {
-    const int gsz = p.group_m * p.n_tiles;
+    const int gsz = p.group_m * sc.n_tiles;
     const int g = r / gsz;
     const int m0 = g * p.group_m;
     const int gm = min(p.group_m, sc.m_tiles - m0);
@@ -436,6 +484,67 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const Sched& sc_,
   mbar_arrive(&tempty[acc]);
 }
 
+// Transposed fp32 tile store for the gradient contractions.  The tile's rows
+// are hidden units (TMEM lane = one output column index m in [0, d)), its
+// columns are output rows n: element (m, n) goes to out[orow(n) * ld_out + m],
+// so for a fixed column the 32 lanes of a warp write 32 consecutive floats.
+//   EPI_DH: n is a compacted row of the chunk; split 0 writes dh at the
+//           original row rowmap[rowmap_base + n], split s >= 1 writes its
+//           partial block out2 + (s-1) * (n_tiles*BN) * ld_out at row n.
+//   EPI_DW: n is a vocabulary row; accumulate adds into the existing dW.
+__device__ __forceinline__ void epi_store_t(const GemmParams& p, const Sched& sc_,
+                                            const TileCoord& c, int acc, uint32_t tmem_row,
+                                            int r_in_tile, uint64_t* tfull, uint64_t* tempty,
+                                            uint32_t use, volatile int* abort_flag, bool& ok) {
+  const int m = c.m * BM + r_in_tile;
+  const bool m_ok = m < sc_.M;
+  const int n0 = c.n * p.BN;
+  const bool mapped = p.rowmap && c.s == 0;
+  float* base = c.s == 0 ? p.out
+                         : p.out2 + static_cast<int64_t>(c.s - 1) * sc_.n_tiles * p.BN * p.ld_out;
+  const bool accum = p.accumulate && c.s == 0;
+  const int kb = c.s * sc_.ks_per_split;
+  const bool kempty = kb >= min(sc_.k_steps, kb + sc_.ks_per_split);
+  const int lane = threadIdx.x & 31;
+  bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
+  ok = __all_sync(0xffffffffu, w);
+  if (!ok) return;
+  tc_fence_after();
+#pragma unroll 1
+  for (int cc = 0; cc < p.BN / 32; ++cc) {
+    const int cb = n0 + cc * 32;
+    if (cb >= sc_.N) break;  // uniform: depends on the tile only
+    uint32_t r[32];
+    if (kempty) {            // nothing accumulated: the tile is zero
+      if (accum) break;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = 0u;
+    } else {
+      tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
+      tmem_ld_wait(r);
+    }
+    // output row of column cb + lane, shared across the warp by shuffles
+    // (every lane takes part; m_ok is warp-uniform because d % 64 == 0)
+    int my_row = cb + lane;
+    if (mapped && cb + lane < sc_.N) my_row = p.rowmap[p.rowmap_base + cb + lane];
+    int orow[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) orow[j] = __shfl_sync(0xffffffffu, my_row, j);
+    const int ncols = min(32, sc_.N - cb);
+    if (m_ok) {
+      float o[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        o[j] = (accum && j < ncols) ? base[static_cast<int64_t>(orow[j]) * p.ld_out + m] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (j < ncols) base[static_cast<int64_t>(orow[j]) * p.ld_out + m] = __uint_as_float(r[j]) + o[j];
+    }
+  }
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int MODE>
@@ -496,8 +605,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         epi_fwd(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else if (MODE == EPI_DZ)
         epi_dz(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
-      else
+      else if (MODE == EPI_STORE)
         epi_store(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+      else
+        epi_store_t(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       if (!ok) break;
     }
   }
@@ -695,12 +806,19 @@ __global__ void kd_gather_rows_kernel(const uint4* __restrict__ h, const int* __
 }
 
 // Split-K completion for dh rows of a chunk: dh[rowmap[c0 + r]] += sum_s part[s][r]
-// in a fixed order, for the chunk's rows r < clamp(*nvalid - c0, 0, cap).  d4 = d / 4.
+// in a fixed order, for the chunk's rows r < clamp(*nvalid - c0, 0, cap).  The
+// contraction published its split count S and partial block height (rows) in
+// split_info; partial s (s < S - 1) starts at part + s * height * 4 * d4.
+// d4 = d / 4.
 __global__ void kd_split_reduce_rows_kernel(float* __restrict__ dh, const float* __restrict__ part,
-                                            int nparts, const int* __restrict__ rowmap,
+                                            const int* __restrict__ split_info,
+                                            const int* __restrict__ rowmap,
                                             const int* __restrict__ nvalid, int c0, int cap,
-                                            int d4, int64_t stride) {
+                                            int d4) {
   const int rows = max(0, min(*nvalid - c0, cap));
+  const int nparts = split_info[0] - 1;
+  if (nparts <= 0) return;
+  const int64_t stride4 = static_cast<int64_t>(split_info[1]) * d4;
   const int64_t n = static_cast<int64_t>(rows) * d4;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -709,7 +827,7 @@ __global__ void kd_split_reduce_rows_kernel(float* __restrict__ dh, const float*
     float4* dst = reinterpret_cast<float4*>(dh) + static_cast<int64_t>(rowmap[c0 + r]) * d4 + j;
     float4 a = *dst;
     for (int s = 0; s < nparts; ++s) {
-      const float4 b = reinterpret_cast<const float4*>(part + s * stride)[i];
+      const float4 b = reinterpret_cast<const float4*>(part)[s * stride4 + i];
       a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
     }
     *dst = a;
