@@ -30,7 +30,11 @@ __all__ = [
     "kd_topk_kl_workspace_size", "kd_topk_kl_launch_count", "kd_topk_kl_forward",
     "kd_topk_kl_forward_noalloc", "kd_topk_kl_backward",
     "kd_gemm_bf16_diag", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
+    "KERNELS", "kd_timing_start", "kd_timing_stop", "kd_timing_query", "kd_timing_release",
 ]
+
+# contraction kernel ids of the diagnostic timing interface
+KERNELS = {"logits_fwd": 0, "logits_bwd": 1, "dh": 3, "dW": 4}
 
 KD_OK = 0
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -76,6 +80,14 @@ def lib() -> ctypes.CDLL:
         L.kd_gemm_bf16_diag.restype = ctypes.c_int
         L.kd_pipeline_wait_selftest.argtypes = [ctypes.c_uint64, vp, vp]
         L.kd_pipeline_wait_selftest.restype = ctypes.c_int
+        L.kd_timing_start.argtypes = [i32]
+        L.kd_timing_start.restype = ctypes.c_int
+        L.kd_timing_stop.argtypes = []
+        L.kd_timing_stop.restype = ctypes.c_int
+        L.kd_timing_query.argtypes = [i32, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_double)]
+        L.kd_timing_query.restype = ctypes.c_int
+        L.kd_timing_release.argtypes = []
+        L.kd_timing_release.restype = ctypes.c_int
         _LIB = L
     return _LIB
 
@@ -166,6 +178,27 @@ def kd_gemm_bf16_diag(A, B, C, M, N, Kd, a_mn, b_mn, *, dev_status, stream=None)
 def kd_pipeline_wait_selftest(limit_ns, *, dev_status, stream=None):
     rc = lib().kd_pipeline_wait_selftest(int(limit_ns), _ptr(dev_status), _stream(stream))
     _check(rc, "kd_pipeline_wait_selftest")
+
+
+def kd_timing_start(capacity: int):
+    """Start bracketing each contraction launch with CUDA events (diagnostic)."""
+    _check(lib().kd_timing_start(int(capacity)), "kd_timing_start")
+
+
+def kd_timing_stop():
+    _check(lib().kd_timing_stop(), "kd_timing_stop")
+
+
+def kd_timing_query(kernel: int):
+    """(launches, total milliseconds) of the recorded launches of one kernel id."""
+    n, ms = ctypes.c_int32(0), ctypes.c_double(0.0)
+    _check(lib().kd_timing_query(int(kernel), ctypes.byref(n), ctypes.byref(ms)),
+           "kd_timing_query")
+    return n.value, ms.value
+
+
+def kd_timing_release():
+    _check(lib().kd_timing_release(), "kd_timing_release")
 
 
 def check_device_status(dev_status, where: str = "device"):

@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <mutex>
+#include <vector>
 
 #include "../../include/kd_topk_kl.h"
 #include "kd_kernels.cuh"
@@ -156,6 +157,49 @@ GemmParams base_params(int a_mn, int b_mn, int BN) {
   return p;
 }
 
+static_assert(KD_KERNEL_LOGITS_FWD == EPI_FWD && KD_KERNEL_LOGITS_BWD == EPI_DZ &&
+                  KD_KERNEL_DH == EPI_DH && KD_KERNEL_DW == EPI_DW,
+              "kernel ids of the timing interface follow the epilogue modes");
+
+// Diagnostic launch timing (kd_timing_*): while recording, each contraction
+// launch is bracketed by two CUDA events on its stream.
+struct TimingRec {
+  int kind;
+  cudaEvent_t start, stop;
+};
+
+struct Timing {
+  std::mutex mu;
+  bool recording = false;
+  int capacity = 0;
+  int used = 0;
+  std::vector<TimingRec> recs;
+};
+
+Timing& timing() {
+  static Timing t;
+  return t;
+}
+
+void destroy_timing_events(Timing& t) {
+  for (auto& r : t.recs) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  t.recs.clear();
+  t.used = 0;
+  t.capacity = 0;
+}
+
+// Slot for the next timed launch, or -1 when not recording / out of slots.
+int timing_slot(int kind) {
+  Timing& t = timing();
+  std::lock_guard<std::mutex> lock(t.mu);
+  if (!t.recording || t.used >= t.capacity) return -1;
+  t.recs[t.used].kind = kind;
+  return t.used++;
+}
+
 template <int MODE>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, GemmParams p, int sms,
                 cudaStream_t st) {
@@ -165,8 +209,14 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, GemmParams p, int sm
                            static_cast<int>(smem)) != cudaSuccess)
     return KD_ERR_CUDA;
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+  const int slot = MODE == EPI_STORE ? -1 : timing_slot(MODE);
+  if (slot >= 0 && cudaEventRecord(timing().recs[slot].start, st) != cudaSuccess)
+    return KD_ERR_CUDA;
   kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
-  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+  if (slot >= 0 && cudaEventRecord(timing().recs[slot].stop, st) != cudaSuccess)
+    return KD_ERR_CUDA;
+  return KD_OK;
 }
 
 struct Ws {
@@ -541,6 +591,64 @@ int kd_topk_kl_forward_noalloc(const void* h, const void* W, const int32_t* teac
   return kd_topk_kl_forward(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, 1, loss,
                             lse, row_kl, gathered_idx, ws, kNoAllocScratchBytes, dev_status,
                             stream);
+}
+
+
+int kd_timing_start(int32_t capacity) {
+  if (capacity < 1 || capacity > 1000000) return KD_ERR_INVALID_ARG;
+  Timing& t = timing();
+  std::lock_guard<std::mutex> lock(t.mu);
+  destroy_timing_events(t);
+  t.recs.resize(static_cast<size_t>(capacity));
+  for (int i = 0; i < capacity; ++i) {
+    t.recs[i].kind = -1;
+    if (cudaEventCreate(&t.recs[i].start) != cudaSuccess ||
+        cudaEventCreate(&t.recs[i].stop) != cudaSuccess) {
+      t.recs.resize(static_cast<size_t>(i));  // keep only fully created pairs
+      destroy_timing_events(t);
+      t.recording = false;
+      return KD_ERR_CUDA;
+    }
+  }
+  t.capacity = capacity;
+  t.used = 0;
+  t.recording = true;
+  return KD_OK;
+}
+
+int kd_timing_stop(void) {
+  Timing& t = timing();
+  std::lock_guard<std::mutex> lock(t.mu);
+  t.recording = false;
+  return KD_OK;
+}
+
+int kd_timing_query(int32_t kernel, int32_t* launches, double* total_ms) {
+  if (!launches || !total_ms) return KD_ERR_INVALID_ARG;
+  Timing& t = timing();
+  std::lock_guard<std::mutex> lock(t.mu);
+  int n = 0;
+  double ms = 0.0;
+  for (int i = 0; i < t.used; ++i) {
+    if (t.recs[i].kind != kernel) continue;
+    if (cudaEventSynchronize(t.recs[i].stop) != cudaSuccess) return KD_ERR_CUDA;
+    float e = 0.f;
+    if (cudaEventElapsedTime(&e, t.recs[i].start, t.recs[i].stop) != cudaSuccess)
+      return KD_ERR_CUDA;
+    ++n;
+    ms += e;
+  }
+  *launches = n;
+  *total_ms = ms;
+  return KD_OK;
+}
+
+int kd_timing_release(void) {
+  Timing& t = timing();
+  std::lock_guard<std::mutex> lock(t.mu);
+  t.recording = false;
+  destroy_timing_events(t);
+  return KD_OK;
 }
 
 }  // extern "C"

@@ -188,6 +188,37 @@ int kd_topk_kl_forward_noalloc(const void* h, const void* W, const int32_t* teac
                                float* row_kl, int32_t* gathered_idx, int32_t* dev_status,
                                struct CUstream_st* stream);
 
+/*
+ * Diagnostic launch timing, for measurement only (the pages describe no such
+ * facility).  Contraction kernels are identified by these ids:
+ *   KD_KERNEL_LOGITS_FWD  forward logit tiles with the lse / gather epilogue
+ *   KD_KERNEL_LOGITS_BWD  backward logit recompute with the gradient epilogue
+ *   KD_KERNEL_DH          dh = G W (computed as dh^T = W^T G^T)
+ *   KD_KERNEL_DW          dW = G^T h (computed as dW^T = h^T G)
+ *
+ * kd_timing_start(capacity): creates 2 x capacity CUDA events on the current
+ *   device (no device memory is allocated) and starts recording: from then on
+ *   every contraction launch that kd_topk_kl_forward / kd_topk_kl_backward
+ *   make, from any host thread, is bracketed by an event pair recorded on its
+ *   stream, until `capacity` launches have been recorded.  Restarting discards
+ *   earlier records.
+ * kd_timing_stop(): stops recording; the records stay readable.
+ * kd_timing_query(kernel, *launches, *total_ms): waits for the recorded
+ *   launches of that kernel id and returns their count and summed duration.
+ * kd_timing_release(): stops recording and destroys the events.
+ * One recorder per process; the calls are serialised internally.
+ */
+enum {
+  KD_KERNEL_LOGITS_FWD = 0,
+  KD_KERNEL_LOGITS_BWD = 1,
+  KD_KERNEL_DH = 3,
+  KD_KERNEL_DW = 4
+};
+int kd_timing_start(int32_t capacity);
+int kd_timing_stop(void);
+int kd_timing_query(int32_t kernel, int32_t* launches, double* total_ms);
+int kd_timing_release(void);
+
 #ifdef __cplusplus
 }
 #endif

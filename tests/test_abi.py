@@ -130,3 +130,13 @@ def test_diag_and_selftest_arg_checks():
     assert L.kd_pipeline_wait_selftest(0, vp(A), None) == INVALID
     assert L.kd_pipeline_wait_selftest(2_000_000_000, vp(A), None) == INVALID
     assert L.kd_pipeline_wait_selftest(1000, None, None) == INVALID
+
+
+def test_timing_interface_without_records():
+    """Querying before anything was recorded returns zero launches and makes no
+    CUDA call; a bad capacity is rejected before any CUDA call."""
+    assert kd.lib().kd_timing_start(0) == INVALID
+    assert kd.lib().kd_timing_stop() == OK
+    for kernel in kd.KERNELS.values():
+        assert kd.kd_timing_query(kernel) == (0, 0.0)
+    assert kd.lib().kd_timing_release() == OK
