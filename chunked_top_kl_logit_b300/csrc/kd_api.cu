@@ -57,6 +57,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 matrix of `outer` rows with `inner` contiguous elements (pitch `ld`),
+// box = box_inner x box_outer, no swizzle: the dW output of the TMA
+// store / reduce-add epilogue.
+bool make_map_f32(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_t ld,
+                  uint32_t box_inner, uint32_t box_outer) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 4};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int device_sms(int* sms) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return KD_ERR_CUDA;
@@ -200,11 +216,13 @@ int timing_slot(int kind) {
   return t.used++;
 }
 
+// `c` is the output tensor map of EPI_DW (ignored by the other modes).
 template <int MODE>
-int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, GemmParams p, int sms,
-                cudaStream_t st) {
+int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, GemmParams p,
+                int sms, cudaStream_t st) {
   if (p.num_tiles <= 0) return KD_OK;
-  const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + 256;
+  p.epi_smem = MODE == EPI_DW ? 4u * 2u * DW_PIECE_FLOATS * 4u : 0u;
+  const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + p.epi_smem + 256;
   if (cudaFuncSetAttribute(kd_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return KD_ERR_CUDA;
@@ -212,7 +230,7 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, GemmParams p, int sm
   const int slot = MODE == EPI_STORE ? -1 : timing_slot(MODE);
   if (slot >= 0 && cudaEventRecord(timing().recs[slot].start, st) != cudaSuccess)
     return KD_ERR_CUDA;
-  kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, p);
+  kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, c, p);
   if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
   if (slot >= 0 && cudaEventRecord(timing().recs[slot].stop, st) != cudaSuccess)
     return KD_ERR_CUDA;
@@ -378,7 +396,7 @@ int kd_topk_kl_forward(const void* h, const void* W, const int32_t* teacher_idx,
   p.part = part;
   p.zg = zg;
   p.gidx = gathered_idx;
-  if ((rc = launch_gemm<EPI_FWD>(ta, tb, p, sms, st))) return rc;
+  if ((rc = launch_gemm<EPI_FWD>(ta, tb, ta, p, sms, st))) return rc;
 
   const int nb = static_cast<int>(cdiv(T, 256));
   kd_combine_kernel<<<nb, 256, 0, st>>>(part, p.n_tiles, static_cast<int>(T), K, w.sp, zg,
@@ -457,7 +475,7 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     p.dyn_kind = 1;
     p.rowmap = rowmap;
     p.rowmap_base = static_cast<int>(c0);
-    if ((rc = launch_gemm<EPI_DZ>(ta, tb, p, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_DZ>(ta, tb, ta, p, sms, st))) return rc;
 
     // (2) dh rows of the chunk, computed transposed: dh_c^T = W^T G_c^T, so a
     // tile is 128 hidden units x 256 chunk rows (A = W as an MN-major operand,
@@ -489,7 +507,7 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     q.part_rows = static_cast<int>(L.part_rows);
     q.policy_sms = kPolicySMs;
     q.split_info = split_info;
-    if ((rc = launch_gemm<EPI_DH>(ta, tb, q, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_DH>(ta, tb, ta, q, sms, st))) return rc;
     if (S > 1) {
       kd_split_reduce_rows_kernel<<<gblocks, 256, 0, st>>>(
           dh, dhpart, split_info, rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
@@ -500,7 +518,10 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     // (3) dW (+)= G_c^T h_c, computed transposed: dW^T = h_c^T G_c with tiles of
     // 128 hidden units x 256 vocabulary rows (both operands MN-major), the
     // contraction running over the chunk's valid rows.
-    if (!make_map(&ta, hc, d, C, d, 64) || !make_map(&tb, dz, V, C, V, 64)) return KD_ERR_CUDA;
+    CUtensorMap tc;
+    if (!make_map(&ta, hc, d, C, d, 64) || !make_map(&tb, dz, V, C, V, 64) ||
+        !make_map_f32(&tc, dW, d, V, d, 32, 32))
+      return KD_ERR_CUDA;
     GemmParams r = base_params(1, 1, kGradBN);
     r.m_tiles = static_cast<int>(cdiv(d, BM));
     r.n_tiles = static_cast<int>(cdiv(V, kGradBN));
@@ -520,7 +541,7 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     r.dyn_base = static_cast<int>(c0);
     r.dyn_cap = static_cast<int>(C);
     r.dyn_kind = 2;
-    if ((rc = launch_gemm<EPI_DW>(ta, tb, r, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_DW>(ta, tb, tc, r, sms, st))) return rc;
   }
   return KD_OK;
 }
@@ -559,7 +580,7 @@ int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t
   p.out = C;
   p.ld_out = N;
   if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
-  return launch_gemm<EPI_STORE>(ta, tb, p, sms, st);
+  return launch_gemm<EPI_STORE>(ta, tb, ta, p, sms, st);
 }
 
 int kd_pipeline_wait_selftest(uint64_t limit_ns, int32_t* dev_status,

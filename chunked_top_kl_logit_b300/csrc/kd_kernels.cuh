@@ -53,6 +53,7 @@ struct GemmParams {
   int a_mn, b_mn;     // 0: K-major tile, 1: MN-major tile
   int BN;             // tile width (MMA N)
   int stages;
+  uint32_t epi_smem;  // shared-memory bytes of the epilogue's staging buffers (EPI_DW)
   uint32_t a_bytes, b_bytes, stage_bytes;
   uint32_t idesc;
   // epilogue, all modes
@@ -545,16 +546,77 @@ __device__ __forceinline__ void epi_store_t(const GemmParams& p, const Sched& sc
   mbar_arrive(&tempty[acc]);
 }
 
+// dW epilogue (EPI_DW): dW^T tile = h^T G, rows = hidden units, columns =
+// vocabulary rows.  Each epilogue warp owns 32 hidden units and moves its part
+// of the tile 32 vocabulary rows at a time through its own two 4 KB staging
+// buffers; one lane then hands the piece to the TMA: a tensor store for the
+// first chunk, a tensor reduce-add (the L2 adds it to dW) for later chunks.
+// Each output element has exactly one owner per launch, so the sum is
+// deterministic.  No barrier spans warps, so a warp that leaves early on an
+// abort cannot leave another waiting.
+constexpr int DW_PIECE_FLOATS = 32 * 32;
+
+__device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, const TileCoord& c,
+                                       int acc, uint32_t tmem_row, int q, uint64_t* tfull,
+                                       uint64_t* tempty, uint32_t use, volatile int* abort_flag,
+                                       bool& ok, const CUtensorMap* tmC, float* stage_buf,
+                                       uint32_t& piece) {
+  const int lane = threadIdx.x & 31;
+  const int mw = c.m * BM + q * 32;       // first hidden unit of this warp
+  const bool warp_ok = mw < sc_.M;        // d % 64 == 0: the warp is all in or all out
+  const int n0 = c.n * p.BN;
+  const bool accum = p.accumulate != 0;
+  const bool kempty = sc_.k_steps == 0;   // no valid row in this chunk
+  bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
+  ok = __all_sync(0xffffffffu, w);
+  if (!ok) return;
+  tc_fence_after();
+#pragma unroll 1
+  for (int cc = 0; cc < p.BN / 32; ++cc) {
+    const int cb = n0 + cc * 32;
+    if (cb >= sc_.N || !warp_ok || (kempty && accum)) break;  // warp-uniform
+    uint32_t r[32];
+    if (kempty) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) r[j] = 0u;
+    } else {
+      tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
+      tmem_ld_wait(r);
+    }
+    float* buf = stage_buf + (piece & 1u) * DW_PIECE_FLOATS;
+    if (lane == 0) bulk_wait_group_read<1>();  // the copy from this buffer two pieces ago is done
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) buf[j * 32 + lane] = __uint_as_float(r[j]);  // [v][m] rows of 128 B
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      if (accum)
+        tma_reduce_add_2d(tmC, buf, mw, cb);
+      else
+        tma_store_2d(tmC, buf, mw, cb);
+      bulk_commit_group();
+    }
+    ++piece;
+  }
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
+  // [pipeline stages][epilogue staging (EPI_DW)][barriers, TMEM slot, abort flag]
+  float* epi_stage = reinterpret_cast<float*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes +
+                                               p.epi_smem);
   uint64_t* empty = full + MAX_STAGES;
   uint64_t* tfull = empty + MAX_STAGES;
   uint64_t* tempty = tfull + 2;
@@ -597,11 +659,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem_row = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     bool ok = true;
     int lt = 0;
+    uint32_t piece = 0;
+    float* my_stage = epi_stage + q * 2 * DW_PIECE_FLOATS;
+    if (MODE == EPI_DW && lane == 0) tma_prefetch_desc(&tmC);
     for (int t = blockIdx.x; t < sc.num_tiles; t += gridDim.x, ++lt) {
       const TileCoord c = decode_tile(p, sc, t);
       const int acc = lt & 1;
       const uint32_t use = static_cast<uint32_t>(lt >> 1);
-      if (MODE == EPI_FWD)
+      if (MODE == EPI_DW)
+        epi_dw(p, sc, c, acc, tmem_row, q, tfull, tempty, use, abort_flag, ok, &tmC, my_stage,
+               piece);
+      else if (MODE == EPI_FWD)
         epi_fwd(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else if (MODE == EPI_DZ)
         epi_dz(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
@@ -611,6 +679,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         epi_store_t(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       if (!ok) break;
     }
+    // the TMA copies this warp issued finish before the CTA leaves
+    if (MODE == EPI_DW && lane == 0) bulk_wait_group_all();
   }
   tc_fence_before();
   __syncthreads();
