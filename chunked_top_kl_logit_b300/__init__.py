@@ -28,7 +28,8 @@ import torch
 __all__ = [
     "KD_OK", "KDError", "lib", "library_path", "status_string",
     "kd_topk_kl_workspace_size", "kd_topk_kl_launch_count", "kd_topk_kl_forward",
-    "kd_topk_kl_forward_noalloc", "kd_topk_kl_backward",
+    "kd_topk_kl_forward_noalloc", "kd_topk_kl_backward", "kd_topk_kl_forward_backward",
+    "KD_ACCUMULATE_DW", "kd_entropy_filter_workspace_size", "kd_entropy_filter",
     "kd_gemm_bf16_diag", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
     "KERNELS", "kd_timing_start", "kd_timing_stop", "kd_timing_query", "kd_timing_release",
 ]
@@ -37,6 +38,7 @@ __all__ = [
 KERNELS = {"logits_fwd": 0, "logits_bwd": 1, "dh": 3, "dW": 4}
 
 KD_OK = 0
+KD_ACCUMULATE_DW = 1
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
 
@@ -71,6 +73,14 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, f32, i64,
                                           vp, f32, vp, vp, vp, sz, vp, vp]
         L.kd_topk_kl_backward.restype = ctypes.c_int
+        L.kd_topk_kl_forward_backward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, f32, i64,
+                                                  f32, ctypes.c_uint32, vp, vp, vp, vp, vp, vp,
+                                                  sz, vp, vp]
+        L.kd_topk_kl_forward_backward.restype = ctypes.c_int
+        L.kd_entropy_filter_workspace_size.argtypes = [i64, ctypes.POINTER(sz)]
+        L.kd_entropy_filter_workspace_size.restype = ctypes.c_int
+        L.kd_entropy_filter.argtypes = [vp, vp, i64, i32, f32, i32, i32, vp, vp, vp, sz, vp, vp]
+        L.kd_entropy_filter.restype = ctypes.c_int
         L.kd_topk_kl_status_string.argtypes = [ctypes.c_int]
         L.kd_topk_kl_status_string.restype = ctypes.c_char_p
         L.kd_topk_kl_forward_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, f32,
@@ -169,6 +179,39 @@ def kd_topk_kl_backward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, ls
     _check(rc, "kd_topk_kl_backward")
 
 
+def kd_topk_kl_forward_backward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, grad_loss,
+                                loss, lse, dh, dW, row_kl=None, *, flags=0, ws, dev_status,
+                                stream=None):
+    """Forward + backward in one call (one teacher prep); flags: KD_ACCUMULATE_DW."""
+    T, d = h.shape
+    V = W.shape[0]
+    K = teacher_idx.shape[1]
+    rc = lib().kd_topk_kl_forward_backward(
+        _ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits), _ptr(valid), T, V, d, K,
+        float(tau), int(chunk), float(grad_loss), int(flags), _ptr(loss), _ptr(lse), _ptr(row_kl),
+        _ptr(dh), _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+        _stream(stream))
+    _check(rc, "kd_topk_kl_forward_backward")
+
+
+def kd_entropy_filter_workspace_size(T: int) -> int:
+    b = ctypes.c_size_t(0)
+    _check(lib().kd_entropy_filter_workspace_size(T, ctypes.byref(b)),
+           "kd_entropy_filter_workspace_size")
+    return b.value
+
+
+def kd_entropy_filter(teacher_logits, valid_in, tau, keep_num, keep_den, valid_out,
+                      entropy=None, *, ws, dev_status, stream=None):
+    """Keep the ceil(N_in * keep_num / keep_den) highest-entropy valid rows."""
+    T, K = teacher_logits.shape
+    rc = lib().kd_entropy_filter(_ptr(teacher_logits), _ptr(valid_in), T, K, float(tau),
+                                 int(keep_num), int(keep_den), _ptr(valid_out), _ptr(entropy),
+                                 _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+                                 _stream(stream))
+    _check(rc, "kd_entropy_filter")
+
+
 def kd_gemm_bf16_diag(A, B, C, M, N, Kd, a_mn, b_mn, *, dev_status, stream=None):
     rc = lib().kd_gemm_bf16_diag(_ptr(A), _ptr(B), _ptr(C), M, N, Kd, int(a_mn), int(b_mn),
                                  _ptr(dev_status), _stream(stream))
@@ -229,6 +272,15 @@ class TopKKL:
                            self.row_kl if row_kl else None, gathered_idx, ws=self.ws,
                            dev_status=self.status, stream=stream)
         return self.loss
+
+    def forward_backward(self, h, W, idx, tl, valid, tau, grad_loss=1.0, accumulate_dW=False,
+                         row_kl=True, stream=None):
+        kd_topk_kl_forward_backward(h, W, idx, tl, valid, tau, self.chunk, grad_loss, self.loss,
+                                    self.lse, self.dh, self.dW,
+                                    self.row_kl if row_kl else None,
+                                    flags=KD_ACCUMULATE_DW if accumulate_dW else 0, ws=self.ws,
+                                    dev_status=self.status, stream=stream)
+        return self.loss, self.dh, self.dW
 
     def backward(self, h, W, idx, tl, valid, tau, grad_loss=1.0, stream=None):
         kd_topk_kl_backward(h, W, idx, tl, valid, tau, self.chunk, self.lse, grad_loss,

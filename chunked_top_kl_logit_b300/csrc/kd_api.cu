@@ -11,6 +11,7 @@
 #include <vector>
 
 #include "../../include/kd_topk_kl.h"
+#include "kd_filter.cuh"
 #include "kd_kernels.cuh"
 
 using namespace kd;
@@ -356,30 +357,21 @@ int kd_topk_kl_launch_count(int64_t T, int64_t V, int64_t d, int32_t K, int64_t 
   return KD_OK;
 }
 
-int kd_topk_kl_forward(const void* h, const void* W, const int32_t* teacher_idx,
-                       const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
-                       int64_t d, int32_t K, float tau, int64_t chunk, float* loss, float* lse,
-                       float* row_kl, int32_t* gathered_idx, void* ws, size_t ws_bytes,
-                       int32_t* dev_status, struct CUstream_st* stream) {
-  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
-                        dev_status);
-  if (rc != KD_OK) return rc;
-  if (!loss || !lse) return KD_ERR_INVALID_ARG;
-  const Layout L = make_layout(T, V, d, K, chunk);
-  if (ws_bytes < L.fwd_total) return KD_ERR_WORKSPACE;
-  int sms = 0;
-  if ((rc = device_sms(&sms)) != KD_OK) return rc;
-  if (!encode_fn()) return KD_ERR_CUDA;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const Ws w = carve(ws, L);
+}  // extern "C"
+
+namespace {
+
+// The forward's launches after the teacher prep: logit GEMM with the lse /
+// gather epilogue, combine, loss.  lse may be null (loss-only evaluation).
+int enqueue_forward(const void* h, const void* W, const uint8_t* valid, int64_t T, int64_t V,
+                    int64_t d, int32_t K, float tau, const Layout& L, void* ws, const Ws& w,
+                    int sms, float* loss, float* lse, float* row_kl, int32_t* gathered_idx,
+                    int32_t* dev_status, cudaStream_t st) {
+  int rc = KD_OK;
   char* wb = static_cast<char*>(ws);
   float* zg = reinterpret_cast<float*>(wb + L.zg);
   float* part = reinterpret_cast<float*>(wb + L.part);
   const float inv_tau = 1.0f / tau;
-
-  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, inv_tau, w, dev_status, st)))
-    return rc;
-
   CUtensorMap ta, tb;
   if (!make_map(&ta, h, d, T, d, BM) || !make_map(&tb, W, d, V, d, ZBN)) return KD_ERR_CUDA;
   GemmParams p = base_params(0, 0, ZBN);
@@ -405,23 +397,15 @@ int kd_topk_kl_forward(const void* h, const void* W, const int32_t* teacher_idx,
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
-int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx,
-                        const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
-                        int64_t d, int32_t K, float tau, int64_t chunk, const float* lse,
-                        float grad_loss, float* dh, float* dW, void* ws, size_t ws_bytes,
-                        int32_t* dev_status, struct CUstream_st* stream) {
-  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
-                        dev_status);
-  if (rc != KD_OK) return rc;
-  if (!lse || !dh || !dW || !aligned16(dh) || !aligned16(dW)) return KD_ERR_INVALID_ARG;
-  if (!std::isfinite(grad_loss)) return KD_ERR_INVALID_ARG;
-  const Layout L = make_layout(T, V, d, K, chunk);
-  if (ws_bytes < L.bwd_total) return KD_ERR_WORKSPACE;
-  int sms = 0;
-  if ((rc = device_sms(&sms)) != KD_OK) return rc;
-  if (!encode_fn()) return KD_ERR_CUDA;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const Ws w = carve(ws, L);
+// The backward's launches after the teacher prep: dh zeroing, row
+// compaction, then per chunk of valid rows the recompute, dh and dW
+// contractions.  accumulate_dW: the first chunk adds to dW instead of
+// overwriting it.
+int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t T, int64_t V,
+                     int64_t d, int32_t K, float tau, const Layout& L, void* ws, const Ws& w,
+                     int sms, const float* lse, float grad_loss, float* dh, float* dW,
+                     int accumulate_dW, int32_t* dev_status, cudaStream_t st) {
+  int rc = KD_OK;
   char* wb = static_cast<char*>(ws);
   int* rowmap = reinterpret_cast<int*>(wb + L.rowmap);
   __nv_bfloat16* hc = reinterpret_cast<__nv_bfloat16*>(wb + L.hc);
@@ -437,8 +421,6 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
   // order.  Their count stays on the device; every kernel clamps to it.
   if (cudaMemsetAsync(dh, 0, static_cast<size_t>(T * d) * sizeof(float), st) != cudaSuccess)
     return KD_ERR_CUDA;
-  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, inv_tau, w, dev_status, st)))
-    return rc;
   kd_compact_rows_kernel<<<1, 1024, 0, st>>>(valid, static_cast<int>(T), rowmap);
   if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
 
@@ -536,7 +518,7 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     r.out = dW;
     r.out2 = nullptr;
     r.ld_out = d;
-    r.accumulate = c0 > 0 ? 1 : 0;
+    r.accumulate = (c0 > 0 || accumulate_dW) ? 1 : 0;
     r.dyn_count = w.nvalid;
     r.dyn_base = static_cast<int>(c0);
     r.dyn_cap = static_cast<int>(C);
@@ -544,6 +526,86 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
     if ((rc = launch_gemm<EPI_DW>(ta, tb, tc, r, sms, st))) return rc;
   }
   return KD_OK;
+}
+
+
+}  // namespace
+
+extern "C" {
+
+int kd_topk_kl_forward(const void* h, const void* W, const int32_t* teacher_idx,
+                       const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
+                       int64_t d, int32_t K, float tau, int64_t chunk, float* loss, float* lse,
+                       float* row_kl, int32_t* gathered_idx, void* ws, size_t ws_bytes,
+                       int32_t* dev_status, struct CUstream_st* stream) {
+  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
+                        dev_status);
+  if (rc != KD_OK) return rc;
+  if (!loss) return KD_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, V, d, K, chunk);
+  if (ws_bytes < L.fwd_total) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Ws w = carve(ws, L);
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, dev_status, st)))
+    return rc;
+  return enqueue_forward(h, W, valid, T, V, d, K, tau, L, ws, w, sms, loss, lse, row_kl,
+                         gathered_idx, dev_status, st);
+}
+
+int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx,
+                        const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
+                        int64_t d, int32_t K, float tau, int64_t chunk, const float* lse,
+                        float grad_loss, float* dh, float* dW, void* ws, size_t ws_bytes,
+                        int32_t* dev_status, struct CUstream_st* stream) {
+  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
+                        dev_status);
+  if (rc != KD_OK) return rc;
+  if (!lse || !dh || !dW || !aligned16(dh) || !aligned16(dW)) return KD_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_loss)) return KD_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, V, d, K, chunk);
+  if (ws_bytes < L.bwd_total) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Ws w = carve(ws, L);
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, dev_status, st)))
+    return rc;
+  return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, sms, lse, grad_loss, dh, dW, 0,
+                          dev_status, st);
+}
+
+int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* teacher_idx,
+                                const float* teacher_logits, const uint8_t* valid, int64_t T,
+                                int64_t V, int64_t d, int32_t K, float tau, int64_t chunk,
+                                float grad_loss, uint32_t flags, float* loss, float* lse,
+                                float* row_kl, float* dh, float* dW, void* ws, size_t ws_bytes,
+                                int32_t* dev_status, struct CUstream_st* stream) {
+  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
+                        dev_status);
+  if (rc != KD_OK) return rc;
+  if (!loss || !lse || !dh || !dW || !aligned16(dh) || !aligned16(dW)) return KD_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_loss) || (flags & ~static_cast<uint32_t>(KD_ACCUMULATE_DW)))
+    return KD_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, V, d, K, chunk);
+  if (ws_bytes < (L.fwd_total > L.bwd_total ? L.fwd_total : L.bwd_total)) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Ws w = carve(ws, L);
+  // one teacher prep serves both passes: the backward's buffers overlay the
+  // forward's lse partials, which the combine has consumed by then
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, dev_status, st)))
+    return rc;
+  if ((rc = enqueue_forward(h, W, valid, T, V, d, K, tau, L, ws, w, sms, loss, lse, row_kl,
+                            nullptr, dev_status, st)))
+    return rc;
+  return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, sms, lse, grad_loss, dh, dW,
+                          (flags & KD_ACCUMULATE_DW) ? 1 : 0, dev_status, st);
 }
 
 int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t Kd,
@@ -670,6 +732,40 @@ int kd_timing_release(void) {
   t.recording = false;
   destroy_timing_events(t);
   return KD_OK;
+}
+
+int kd_entropy_filter_workspace_size(int64_t T, size_t* bytes) {
+  if (T < 1 || !bytes) return KD_ERR_INVALID_ARG;
+  if (T > INT32_MAX) return KD_ERR_UNSUPPORTED;
+  *bytes = al256(static_cast<size_t>(T) * 4);
+  return KD_OK;
+}
+
+int kd_entropy_filter(const float* teacher_logits, const uint8_t* valid_in, int64_t T, int32_t K,
+                      float tau, int32_t keep_num, int32_t keep_den, uint8_t* valid_out,
+                      float* entropy, void* ws, size_t ws_bytes, int32_t* dev_status,
+                      struct CUstream_st* stream) {
+  if (!teacher_logits || !valid_in || !valid_out || !ws || !dev_status) return KD_ERR_INVALID_ARG;
+  if (T < 1 || K < 1 || !(tau > 0.f) || !std::isfinite(tau)) return KD_ERR_INVALID_ARG;
+  if (keep_den < 1 || keep_num < 0 || keep_num > keep_den) return KD_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(teacher_logits) & 3u) ||
+      (reinterpret_cast<uintptr_t>(entropy) & 3u) || (reinterpret_cast<uintptr_t>(ws) & 255u) ||
+      (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+    return KD_ERR_INVALID_ARG;
+  if (T > INT32_MAX || static_cast<double>(T) * K > 2e9) return KD_ERR_UNSUPPORTED;
+  if (ws_bytes < al256(static_cast<size_t>(T) * 4)) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  const int rc = device_sms(&sms);
+  if (rc != KD_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
+  uint32_t* keys = static_cast<uint32_t*>(ws);
+  const int rows_per_block = 8;
+  kd_entropy_kernel<<<static_cast<unsigned>(cdiv(T, rows_per_block)), 32 * rows_per_block, 0,
+                      st>>>(teacher_logits, static_cast<int>(T), K, 1.0f / tau, entropy, keys);
+  kd_entropy_select_kernel<<<1, FILTER_THREADS, 0, st>>>(keys, valid_in, static_cast<int>(T),
+                                                         keep_num, keep_den, valid_out);
+  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
 }  // extern "C"

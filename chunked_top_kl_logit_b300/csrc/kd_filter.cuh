@@ -1,0 +1,158 @@
+// Teacher-entropy token filter: the mask producer in front of the loss.
+//
+// asibiont.com rewrite, "Distillation Token Filtering": score each token by
+// the entropy of the teacher's distribution and, per batch, keep a fixed
+// percentage of the tokens with the highest entropy.  Here the distribution is
+// the renormalised top-K softmax at temperature tau (the one the loss uses),
+// H_t = -sum_k p_tk log p_tk; among rows with valid_in != 0 the
+// n_keep = ceil(N_in * keep_num / keep_den) rows of largest H are kept, equal
+// entropies ordered by row index (lower first).  The selection is exact and
+// deterministic: an MSB-first radix select over order-preserving 32-bit keys
+// of H, then an ordered scan that admits the threshold's ties by row.
+#pragma once
+
+#include <math_constants.h>
+#include <stdint.h>
+
+namespace kd {
+
+// Order-preserving map of a finite float to uint32 (-0 is folded into +0 so
+// that equal values get equal keys).
+__device__ __forceinline__ uint32_t float_order_key(float x) {
+  const uint32_t u = __float_as_uint(x + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// One warp per row: H_t and its key.
+__global__ void kd_entropy_kernel(const float* __restrict__ tl, int T, int K, float inv_tau,
+                                  float* __restrict__ entropy, uint32_t* __restrict__ keys) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;
+  const float* tr = tl + static_cast<int64_t>(row) * K;
+  float m = -CUDART_INF_F;
+  for (int k = lane; k < K; k += 32) m = fmaxf(m, tr[k] * inv_tau);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float S = 0.f;
+  for (int k = lane; k < K; k += 32) S += expf(tr[k] * inv_tau - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  const float logS = logf(S);
+  float H = 0.f;
+  for (int k = lane; k < K; k += 32) {
+    const float lp = tr[k] * inv_tau - m - logS;
+    const float pk = expf(lp);
+    if (pk > 0.f) H -= pk * lp;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) H += __shfl_xor_sync(0xffffffffu, H, o);
+  if (lane == 0) {
+    if (entropy) entropy[row] = H;
+    keys[row] = float_order_key(H);
+  }
+}
+
+constexpr int FILTER_THREADS = 1024;
+
+// Single block: count the candidates, radix-select the n_keep-th largest key
+// among them, then write the mask (ties at the threshold by row order).
+__global__ void __launch_bounds__(FILTER_THREADS, 1)
+    kd_entropy_select_kernel(const uint32_t* __restrict__ keys, const uint8_t* __restrict__ valid_in,
+                             int T, int keep_num, int keep_den, uint8_t* __restrict__ valid_out) {
+  __shared__ uint32_t hist[256];
+  __shared__ int warp_sum[FILTER_THREADS / 32];
+  __shared__ uint32_t s_prefix, s_remaining;
+  __shared__ int s_base;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int wid = tid >> 5;
+
+  // N_in
+  int cnt = 0;
+  for (int t = tid; t < T; t += FILTER_THREADS) cnt += valid_in[t] != 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+  if (lane == 0) warp_sum[wid] = cnt;
+  __syncthreads();
+  if (tid == 0) {
+    long long n_in = 0;
+    for (int w = 0; w < FILTER_THREADS / 32; ++w) n_in += warp_sum[w];
+    const long long n_keep = (n_in * keep_num + keep_den - 1) / keep_den;
+    s_remaining = static_cast<uint32_t>(n_keep);
+    s_prefix = 0u;
+  }
+  __syncthreads();
+  const uint32_t n_keep = s_remaining;
+
+  // radix select, 8 bits per pass from the top: afterwards s_prefix is the key
+  // of the n_keep-th largest candidate and s_remaining the number of rows with
+  // exactly that key that are kept
+  uint32_t mask = 0u;
+  if (n_keep > 0) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += FILTER_THREADS) hist[i] = 0u;
+      __syncthreads();
+      const uint32_t prefix = s_prefix;
+      for (int t = tid; t < T; t += FILTER_THREADS) {
+        const uint32_t k = keys[t];
+        if (valid_in[t] && (k & mask) == prefix) atomicAdd(&hist[(k >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        uint32_t need = s_remaining, cum = 0u;
+        for (int dg = 255; dg >= 0; --dg) {
+          if (cum + hist[dg] >= need) {
+            s_prefix = prefix | (static_cast<uint32_t>(dg) << shift);
+            s_remaining = need - cum;
+            break;
+          }
+          cum += hist[dg];
+        }
+      }
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+  }
+  const uint32_t theta = s_prefix;
+  const uint32_t k_eq = s_remaining;
+
+  // mask: keys above the threshold, and the first k_eq rows (in row order)
+  // whose key equals it
+  if (tid == 0) s_base = 0;
+  __syncthreads();
+  for (int t0 = 0; t0 < T; t0 += FILTER_THREADS) {
+    const int t = t0 + tid;
+    const bool cand = t < T && valid_in[t];
+    const uint32_t k = t < T ? keys[t] : 0u;
+    const int eq = (n_keep > 0 && cand && k == theta) ? 1 : 0;
+    int x = eq;  // inclusive scan of eq over the block, in row order
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sum[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int v = warp_sum[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += y;
+      }
+      warp_sum[lane] = v;
+    }
+    __syncthreads();
+    const int before = s_base + (wid > 0 ? warp_sum[wid - 1] : 0) + x - eq;
+    if (t < T) {
+      const bool keep = n_keep > 0 && cand && (k > theta || (eq && before < static_cast<int>(k_eq)));
+      valid_out[t] = keep ? 1 : 0;
+    }
+    __syncthreads();
+    if (tid == 0) s_base += warp_sum[FILTER_THREADS / 32 - 1];
+    __syncthreads();
+  }
+}
+
+}  // namespace kd

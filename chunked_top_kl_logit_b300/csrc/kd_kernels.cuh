@@ -779,7 +779,7 @@ __global__ void kd_combine_kernel(const float* __restrict__ part, int n_tiles, i
       }
     }
     const float lse = m + logf(s);
-    lse_out[row] = lse;
+    if (lse_out) lse_out[row] = lse;
     float rk = 0.f;
     if (valid[row]) {
       const float* pr = sp + static_cast<int64_t>(row) * K;

@@ -98,7 +98,8 @@ int kd_topk_kl_launch_count(int64_t T, int64_t V, int64_t d, int32_t K, int64_t 
  *
  * Inputs  (device): h, W, teacher_idx, teacher_logits, valid as above.
  * Outputs (device): loss     fp32 scalar
- *                   lse      fp32 [T]   log sum_v exp(z_tv / tau), every row
+ *                   lse      fp32 [T]   log sum_v exp(z_tv / tau), every row;
+ *                            or NULL for a loss-only (evaluation) forward
  *                   row_kl   fp32 [T]   or NULL; 0 for invalid rows
  *                   gathered_idx int32 [T x K] or NULL: for every (t, k), the
  *                            vocabulary column whose logit the kernel read
@@ -131,6 +132,55 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
                         int64_t d, int32_t K, float tau, int64_t chunk, const float* lse,
                         float grad_loss, float* dh, float* dW, void* ws, size_t ws_bytes,
                         int32_t* dev_status, struct CUstream_st* stream);
+
+/*
+ * Forward and backward in one call, for a training step (the aipuls.nl
+ * "Summary" describes the loss as the student's training objective): the
+ * same results as kd_topk_kl_forward followed by kd_topk_kl_backward with the
+ * same arguments, with one teacher prep serving both passes.
+ *
+ * grad_loss: d(objective)/d(loss), as in kd_topk_kl_backward.
+ * flags: 0 or KD_ACCUMULATE_DW.  With KD_ACCUMULATE_DW, dW += G^T h instead of
+ *   dW = G^T h (gradient accumulation over micro-batches); dh is always
+ *   overwritten.
+ * Outputs (device): loss, lse (required), row_kl (or NULL), dh, dW.
+ * ws/ws_bytes: at least max(*fwd_bytes, *bwd_bytes) of
+ *   kd_topk_kl_workspace_size.
+ */
+#define KD_ACCUMULATE_DW 1u
+int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* teacher_idx,
+                                const float* teacher_logits, const uint8_t* valid, int64_t T,
+                                int64_t V, int64_t d, int32_t K, float tau, int64_t chunk,
+                                float grad_loss, uint32_t flags, float* loss, float* lse,
+                                float* row_kl, float* dh, float* dW, void* ws, size_t ws_bytes,
+                                int32_t* dev_status, struct CUstream_st* stream);
+
+/*
+ * Teacher-entropy token filter, the producer of the valid mask (asibiont.com
+ * rewrite, section "Distillation Token Filtering": score each token by the
+ * entropy of the teacher's distribution and keep, per batch, a fixed
+ * percentage of the tokens with the highest entropy).
+ *
+ *   p_tk = softmax_k(teacher_logits_tk / tau) over the K cached entries
+ *   H_t  = -sum_k p_tk log p_tk                      (natural log)
+ *   N_in = number of rows with valid_in != 0
+ *   n_keep = ceil(N_in * keep_num / keep_den)        (exact integer arithmetic)
+ *   valid_out[t] = 1 for the n_keep rows with valid_in != 0 and the largest
+ *                  H_t (equal H_t: the lower row first), else 0.
+ *
+ * Inputs (device): teacher_logits fp32 [T x K] (finite), valid_in uint8 [T].
+ * Outputs (device): valid_out uint8 [T]; entropy fp32 [T] or NULL.
+ * Limits: T >= 1, K >= 1, tau > 0, 0 <= keep_num <= keep_den, keep_den >= 1.
+ * ws/ws_bytes: caller-owned device scratch, 256-byte aligned, at least
+ * kd_entropy_filter_workspace_size(T).  *dev_status is reset to 0 (the filter
+ * raises no device error).  Deterministic: the result depends only on the
+ * inputs.
+ */
+int kd_entropy_filter_workspace_size(int64_t T, size_t* bytes);
+int kd_entropy_filter(const float* teacher_logits, const uint8_t* valid_in, int64_t T, int32_t K,
+                      float tau, int32_t keep_num, int32_t keep_den, uint8_t* valid_out,
+                      float* entropy, void* ws, size_t ws_bytes, int32_t* dev_status,
+                      struct CUstream_st* stream);
 
 /* Static, NUL-terminated description of a kd_status value (never NULL). */
 const char* kd_topk_kl_status_string(int status);

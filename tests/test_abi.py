@@ -95,7 +95,7 @@ def bwd(**kw):
 
 @pytest.mark.parametrize("kw", [dict(h=None), dict(W=None), dict(idx=None), dict(tl=None),
                                 dict(valid=None), dict(ws=None), dict(status=None),
-                                dict(loss=None), dict(lse=None), dict(tau=0.0),
+                                dict(loss=None), dict(tau=0.0),
                                 dict(tau=-1.0), dict(tau=float("inf")), dict(tau=float("nan")),
                                 dict(h=A + 8), dict(W=A + 2), dict(ws=A + 4), dict(idx=A + 2),
                                 dict(T=0), dict(K=0)])
@@ -140,3 +140,17 @@ def test_timing_interface_without_records():
     for kernel in kd.KERNELS.values():
         assert kd.kd_timing_query(kernel) == (0, 0.0)
     assert kd.lib().kd_timing_release() == OK
+
+
+def test_forward_backward_argument_checks():
+    """The fused entry rejects bad flags, a missing lse and a small workspace
+    before any CUDA call."""
+    A = ctypes.c_void_p(0x10000)
+    T, V, d, K, chunk = 64, 1024, 64, 8, 64
+    f, b = kd.kd_topk_kl_workspace_size(T, V, d, K, chunk)
+    L = kd.lib()
+    args = lambda flags, lse, ws_bytes: (A, A, A, A, A, T, V, d, K, 1.0, chunk, 1.0, flags,
+                                         A, lse, None, A, A, A, ws_bytes, A, None)
+    assert L.kd_topk_kl_forward_backward(*args(2, A, max(f, b))) == INVALID
+    assert L.kd_topk_kl_forward_backward(*args(0, None, max(f, b))) == INVALID
+    assert L.kd_topk_kl_forward_backward(*args(0, A, min(f, b) - 1)) == WORKSPACE

@@ -1,0 +1,129 @@
+"""The single-call training step kd_topk_kl_forward_backward, the dW
+accumulation flag and the loss-only forward, through the C ABI.
+
+The fused call runs the same kernels in the same order as the separate
+forward and backward, so its outputs must match them bit for bit; with
+KD_ACCUMULATE_DW, dW must equal the previous contents plus this batch's dW
+(fp32 rounding of the extra addition only); the loss-only forward (lse = NULL)
+must give the same loss.  One case is also held to the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import chunked_top_kl_logit_b300 as kd
+from oracle import kd_oracle as O
+from synth import make_inputs, workload
+from tests.gpu_util import GRAD_RL2, LOSS_RTOL, LSE_ATOL, oracle_inputs, rel_l2, to_device
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    ("T600_V5000_d256_chunk200", dict(T=600, d=256, V=5000, K=50, tau=1.5), 200),
+    ("packed_T520_V3000_d320", dict(T=520, d=320, V=3000, K=64, tau=2.0, mask_kind="packed",
+                                    seq_len=130, pad=30), 1000),
+]
+
+
+def _separate(g, chunk, grad_loss):
+    T, d = g["h"].shape
+    V, K = g["W"].shape[0], g["teacher_idx"].shape[1]
+    m = kd.TopKKL(T, V, d, K, chunk)
+    args = (g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"], g["tau"])
+    m.forward(*args)
+    m.backward(*args, grad_loss)
+    torch.cuda.synchronize()
+    kd.check_device_status(m.status, "separate")
+    return m
+
+
+@pytest.mark.parametrize("name,over,chunk", CASES, ids=[c[0] for c in CASES])
+def test_fused_equals_separate_bitwise(name, over, chunk):
+    x = make_inputs(workload("small_4k", **over))
+    g = to_device(x)
+    a = _separate(g, chunk, 0.75)
+    T, d = g["h"].shape
+    V, K = g["W"].shape[0], g["teacher_idx"].shape[1]
+    b = kd.TopKKL(T, V, d, K, chunk)
+    b.forward_backward(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"], g["tau"],
+                       0.75)
+    torch.cuda.synchronize()
+    kd.check_device_status(b.status, "fused")
+    for k in ("loss", "lse", "row_kl", "dh", "dW"):
+        assert torch.equal(getattr(a, k), getattr(b, k)), k
+
+
+def test_fused_parity_with_oracle():
+    x = make_inputs(workload("small_4k", T=700, d=192, V=6000, K=40, tau=1.0))
+    g = to_device(x)
+    T, d = g["h"].shape
+    V, K = g["W"].shape[0], g["teacher_idx"].shape[1]
+    m = kd.TopKKL(T, V, d, K, 256)
+    m.forward_backward(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"], g["tau"],
+                       1.0)
+    torch.cuda.synchronize()
+    kd.check_device_status(m.status, "fused")
+    P = oracle_inputs(x)
+    args = (P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], P["valid"], P["tau"])
+    f = O.forward(*args)
+    dh, dW = O.backward(*args, 1.0, lse=f["lse"])
+    assert abs(float(m.loss.item()) - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert np.abs(m.lse.double().cpu().numpy() - f["lse"]).max() <= LSE_ATOL
+    assert rel_l2(m.dh.double().cpu().numpy(), dh) <= GRAD_RL2
+    assert rel_l2(m.dW.double().cpu().numpy(), dW) <= GRAD_RL2
+
+
+@pytest.mark.parametrize("chunk", [96, 1000])
+def test_accumulate_dW_adds_to_previous_contents(chunk):
+    x = make_inputs(workload("small_4k", T=500, d=192, V=3000, K=32, tau=1.0, idx_kind="uniform"))
+    g = to_device(x)
+    T, d = g["h"].shape
+    V, K = g["W"].shape[0], g["teacher_idx"].shape[1]
+    ref = _separate(g, chunk, 1.0)
+    m = kd.TopKKL(T, V, d, K, chunk)
+    prev = torch.randn(V, d, device="cuda", generator=torch.Generator("cuda").manual_seed(4))
+    m.dW.copy_(prev)
+    m.forward_backward(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"], g["tau"],
+                       1.0, accumulate_dW=True)
+    torch.cuda.synchronize()
+    kd.check_device_status(m.status, "accumulate")
+    assert torch.equal(m.dh, ref.dh)
+    expect = prev.double() + ref.dW.double()
+    err = (m.dW.double() - expect).abs().max().item()
+    assert err <= 1e-6 * expect.abs().max().item(), err
+    # a second accumulation adds the same dW again
+    m.forward_backward(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"], g["tau"],
+                       1.0, accumulate_dW=True)
+    torch.cuda.synchronize()
+    expect2 = expect + ref.dW.double()
+    assert (m.dW.double() - expect2).abs().max().item() <= 2e-6 * expect2.abs().max().item()
+
+
+def test_accumulate_with_no_valid_rows_leaves_dW():
+    x = make_inputs(workload("small_4k", T=130, d=128, V=1024, K=20, idx_kind="uniform"))
+    x["valid"] = torch.zeros_like(x["valid"])
+    g = to_device(x)
+    m = kd.TopKKL(130, 1024, 128, 20, 64)
+    prev = torch.randn(1024, 128, device="cuda")
+    m.dW.copy_(prev)
+    m.forward_backward(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"], g["tau"],
+                       1.0, accumulate_dW=True)
+    torch.cuda.synchronize()
+    kd.check_device_status(m.status, "accumulate")
+    assert float(m.loss.item()) == 0.0
+    assert torch.equal(m.dW, prev) and bool((m.dh == 0).all())
+
+
+def test_loss_only_forward():
+    x = make_inputs(workload("small_4k", T=300, d=128, V=2000, K=30, tau=1.0))
+    g = to_device(x)
+    a = _separate(g, 128, 1.0)
+    loss = torch.empty(1, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(kd.kd_topk_kl_workspace_size(300, 2000, 128, 30, 128)[0], dtype=torch.uint8,
+                     device="cuda")
+    kd.kd_topk_kl_forward(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"],
+                          g["tau"], 128, loss, None, ws=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(loss, a.loss)

@@ -16,6 +16,7 @@ import os
 import numpy as np
 import pytest
 import scipy.special
+import scipy.stats
 import torch
 
 from oracle import kd_oracle as O
@@ -419,3 +420,80 @@ def test_planted_missing_teacher_scatter(monkeypatch):
     _mutant(monkeypatch, "grad_logits_rows", bad)
     with pytest.raises(AssertionError):
         check_fd(O)
+
+
+# --------------------------------------------------------------------------
+# teacher-entropy token filter (asibiont.com, "Distillation Token Filtering")
+# --------------------------------------------------------------------------
+
+from oracle import entropy_filter as EF  # noqa: E402
+
+
+def test_entropy_closed_forms():
+    K = 7
+    # equal logits: uniform over K entries, H = log K for any tau
+    assert np.allclose(EF.teacher_entropy(np.full((3, K), 2.5), 0.7), math.log(K), atol=1e-14)
+    # one dominant logit: H -> 0
+    tl = np.zeros((1, K))
+    tl[0, 3] = 800.0
+    assert EF.teacher_entropy(tl, 1.0)[0] < 1e-300 or EF.teacher_entropy(tl, 1.0)[0] == 0.0
+    # two entries: binary entropy of sigmoid(a - b)
+    a, b, tau = 1.3, -0.4, 1.7
+    s = 1.0 / (1.0 + math.exp(-(a - b) / tau))
+    hb = -(s * math.log(s) + (1 - s) * math.log(1 - s))
+    assert abs(EF.teacher_entropy(np.array([[a, b]]), tau)[0] - hb) < 1e-14
+    # scipy's entropy of the softmax, as an independent routine
+    rng = np.random.default_rng(3)
+    tl = rng.normal(0, 2, size=(5, 11))
+    ref = scipy.stats.entropy(scipy.special.softmax(tl / 1.3, axis=1), axis=1)
+    assert np.allclose(EF.teacher_entropy(tl, 1.3), ref, atol=1e-13)
+
+
+def test_entropy_temperature_scaling():
+    rng = np.random.default_rng(4)
+    tl = rng.normal(0, 3, size=(6, 9))
+    assert np.allclose(EF.teacher_entropy(tl, 2.0), EF.teacher_entropy(tl / 2.0, 1.0), atol=1e-14)
+    # higher temperature flattens the distribution: entropy does not decrease
+    assert np.all(EF.teacher_entropy(tl, 3.0) >= EF.teacher_entropy(tl, 1.0) - 1e-12)
+
+
+def test_keep_count_exact():
+    assert EF.keep_count(10, 3, 10) == 3
+    assert EF.keep_count(10, 31, 100) == 4
+    assert EF.keep_count(0, 1, 2) == 0
+    assert EF.keep_count(7, 0, 5) == 0
+    assert EF.keep_count(7, 5, 5) == 7
+    for n in range(50):
+        for num, den in ((1, 3), (2, 7), (70, 100)):
+            assert EF.keep_count(n, num, den) == math.ceil(n * num / den - 1e-12)
+
+
+def test_entropy_filter_bruteforce():
+    """Against an exhaustive check: every kept row has (H, -row) above every
+    dropped candidate, the count is exact and non-candidates are never kept."""
+    rng = np.random.default_rng(5)
+    for trial in range(30):
+        T = int(rng.integers(1, 40))
+        H = rng.choice([0.0, 0.5, 1.0, 1.5], size=T) if trial % 2 else rng.random(T)
+        valid = (rng.random(T) < 0.7).astype(np.uint8)
+        num, den = int(rng.integers(0, 11)), 10
+        out = EF.entropy_filter(H, valid, num, den)
+        cand = np.nonzero(valid)[0]
+        assert out.sum() == EF.keep_count(len(cand), num, den)
+        assert np.all(out[valid == 0] == 0)
+        kept = [t for t in cand if out[t]]
+        dropped = [t for t in cand if not out[t]]
+        for a in kept:
+            for b in dropped:
+                assert (H[a] > H[b]) or (H[a] == H[b] and a < b)
+
+
+def test_entropy_filter_extremes():
+    H = np.array([0.3, 0.1, 0.3, 0.9])
+    valid = np.array([1, 1, 0, 1], dtype=np.uint8)
+    assert np.array_equal(EF.entropy_filter(H, valid, 1, 1), valid)
+    assert EF.entropy_filter(H, valid, 0, 1).sum() == 0
+    # one of three: the highest entropy among candidates (row 3)
+    assert np.array_equal(EF.entropy_filter(H, valid, 1, 3), [0, 0, 0, 1])
+    # ties: rows 0 and 2 share H, row 2 is not a candidate; row 0 before row 1
+    assert np.array_equal(EF.entropy_filter(H, valid, 2, 3), [1, 0, 0, 1])
