@@ -411,6 +411,63 @@ def run_ours(args, w, world, rank, local_rank):
     return out
 
 
+def run_entropy_filter(args, w, world, rank, local_rank):
+    """The teacher-entropy token filter on the workload's teacher cache: one
+    step = one kd_entropy_filter call (entropy of every row + exact selection),
+    inputs resident in HBM.  Roofline: HBM, algorithmic bytes = the teacher
+    logits read once + valid_in read + valid_out written."""
+    import chunked_top_kl_logit_b300 as kd
+    from synth import make_inputs
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    x = make_inputs(w.replace(idx_kind="uniform"), seed=args.seed + rank, device=dev)
+    tl = x["teacher_logits"].to(dev)
+    valid = x["valid"].to(dev)
+    T, K = tl.shape
+    out = torch.empty(T, dtype=torch.uint8, device=dev)
+    ent = torch.empty(T, dtype=torch.float32, device=dev)
+    ws = torch.empty(kd.kd_entropy_filter_workspace_size(T), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # 256 MB > L2
+
+    def step():
+        kd.kd_entropy_filter(tl, valid, w.tau, 7, 10, out, ent, ws=ws, dev_status=st)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    n = args.steps
+    e = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n)]
+    barrier(world)
+    for i in range(n):
+        flush.zero_()
+        e[i][0].record()
+        step()
+        e[i][1].record()
+    torch.cuda.synchronize()
+    barrier(world)
+    ms = statistics.mean(a.elapsed_time(b) for a, b in e)
+    max_sec = max_over_ranks(ms / 1e3 * n, world, device=dev)
+    alg_bytes = T * K * 4 + 2 * T
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    gbs = alg_bytes / (ms / 1e3) / 1e9
+    return {
+        "metric": "teacher-entropy token filter rows/s", "op": "entropy_filter",
+        "value": job_throughput(T * n, world, max_sec), "unit": "rows/s", "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": max_sec * 1e3 / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "K": K, "tau": w.tau, "keep": "7/10",
+                   "l2": "256 MB buffer written between timed calls"},
+        "roofline": {"kernel": "kd_entropy_kernel + kd_entropy_select_kernel", "bound": "hbm",
+                     "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "peak_kind": f"HBM copy bandwidth, {src}", "traffic": None,
+                     "bytes_per_launch": alg_bytes},
+        "gpu_launches": 2 * n,
+    }
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,6 +479,9 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--op", default="loss", choices=["loss", "entropy_filter"],
+                    help="loss: the fused top-K KL forward + backward (headline); "
+                         "entropy_filter: the mask producer alone")
     ap.add_argument("--api", default="split", choices=["split", "fused"],
                     help="split: kd_topk_kl_forward + kd_topk_kl_backward per step; "
                          "fused: one kd_topk_kl_forward_backward call per step")
@@ -441,6 +501,13 @@ def main(argv=None):
         return 0
 
     dist_setup(world, "nccl")
+    if args.op == "entropy_filter":
+        out = run_entropy_filter(args, w, world, rank, local_rank)
+        if rank == 0:
+            print(json.dumps(out), flush=True)
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
     out = run_ours(args, w, world, rank, local_rank)
     if rank == 0:
         if world == 1 and not args.no_cpu:

@@ -737,7 +737,7 @@ int kd_timing_release(void) {
 int kd_entropy_filter_workspace_size(int64_t T, size_t* bytes) {
   if (T < 1 || !bytes) return KD_ERR_INVALID_ARG;
   if (T > INT32_MAX) return KD_ERR_UNSUPPORTED;
-  *bytes = al256(static_cast<size_t>(T) * 4);
+  *bytes = al256(static_cast<size_t>(T + 3) / 4 * 16);  // keys, padded to whole uint4
   return KD_OK;
 }
 
@@ -753,7 +753,7 @@ int kd_entropy_filter(const float* teacher_logits, const uint8_t* valid_in, int6
       (reinterpret_cast<uintptr_t>(dev_status) & 3u))
     return KD_ERR_INVALID_ARG;
   if (T > INT32_MAX || static_cast<double>(T) * K > 2e9) return KD_ERR_UNSUPPORTED;
-  if (ws_bytes < al256(static_cast<size_t>(T) * 4)) return KD_ERR_WORKSPACE;
+  if (ws_bytes < al256(static_cast<size_t>(T + 3) / 4 * 16)) return KD_ERR_WORKSPACE;
   int sms = 0;
   const int rc = device_sms(&sms);
   if (rc != KD_OK) return rc;
@@ -762,9 +762,10 @@ int kd_entropy_filter(const float* teacher_logits, const uint8_t* valid_in, int6
   uint32_t* keys = static_cast<uint32_t*>(ws);
   const int rows_per_block = 8;
   kd_entropy_kernel<<<static_cast<unsigned>(cdiv(T, rows_per_block)), 32 * rows_per_block, 0,
-                      st>>>(teacher_logits, static_cast<int>(T), K, 1.0f / tau, entropy, keys);
-  kd_entropy_select_kernel<<<1, FILTER_THREADS, 0, st>>>(keys, valid_in, static_cast<int>(T),
-                                                         keep_num, keep_den, valid_out);
+                      st>>>(teacher_logits, valid_in, static_cast<int>(T), K, 1.0f / tau, entropy,
+                            keys);
+  kd_entropy_select_kernel<<<1, FILTER_THREADS, 0, st>>>(keys, static_cast<int>(T), keep_num,
+                                                         keep_den, valid_out);
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
