@@ -278,15 +278,27 @@ def run_ours(args, w, world, rank, local_rank):
     m = kd.TopKKL(T, V, d, K, chunk, device=dev)
 
     fused = args.api == "fused"
+    residual = args.variant == "residual"
+    if residual:
+        from synth import teacher_full_lse
+        tlse = teacher_full_lse(x["teacher_logits"].cpu(), tau, seed=args.seed + rank).to(dev)
+        topk_mass = torch.empty(T, dtype=torch.float32, device=dev)
 
     def fwd_part():
-        if fused:
+        if residual:
+            kd.kd_topk_kl_forward_residual(h, W, idx, tl, tlse, valid, tau, chunk, m.loss, m.lse,
+                                           m.row_kl, topk_mass, ws=m.ws, dev_status=m.status)
+        elif fused:
             m.forward_backward(h, W, idx, tl, valid, tau, 1.0)
         else:
             m.forward(h, W, idx, tl, valid, tau)
 
     def bwd_part():
-        if not fused:
+        if residual:
+            kd.kd_topk_kl_backward_residual(h, W, idx, tl, tlse, valid, tau, chunk, m.lse,
+                                            topk_mass, 1.0, m.dh, m.dW, ws=m.ws,
+                                            dev_status=m.status)
+        elif not fused:
             m.backward(h, W, idx, tl, valid, tau, 1.0)
 
     def step():
@@ -390,7 +402,7 @@ def run_ours(args, w, world, rank, local_rank):
         "tflops_algorithmic": flops_alg / (ms_per_step / 1e3) / 1e12,
         "frac_bf16_peak_burst": tf_nominal / world / burst,
         "frac_bf16_peak_sustained": tf_nominal / world / sustained,
-        "api": args.api,
+        "api": args.api, "variant": args.variant,
         "fwd_ms": None if fused else fwd_ms, "bwd_ms": None if fused else bwd_ms,
         "kernels": kernels,
         "roofline": {"kernel": f"kd_gemm_kernel<{kd.KERNELS[dom]}> ({KERNEL_DESC[dom]})",
@@ -482,6 +494,9 @@ def main(argv=None):
     ap.add_argument("--op", default="loss", choices=["loss", "entropy_filter"],
                     help="loss: the fused top-K KL forward + backward (headline); "
                          "entropy_filter: the mask producer alone")
+    ap.add_argument("--variant", default="main", choices=["main", "residual"],
+                    help="main: teacher renormalised over its top-K; residual: the teacher's "
+                         "full-vocabulary normaliser and an 'everything else' outcome")
     ap.add_argument("--api", default="split", choices=["split", "fused"],
                     help="split: kd_topk_kl_forward + kd_topk_kl_backward per step; "
                          "fused: one kd_topk_kl_forward_backward call per step")

@@ -30,6 +30,7 @@ __all__ = [
     "kd_topk_kl_workspace_size", "kd_topk_kl_launch_count", "kd_topk_kl_forward",
     "kd_topk_kl_forward_noalloc", "kd_topk_kl_backward", "kd_topk_kl_forward_backward",
     "KD_ACCUMULATE_DW", "kd_entropy_filter_workspace_size", "kd_entropy_filter",
+    "kd_topk_kl_forward_residual", "kd_topk_kl_backward_residual",
     "kd_gemm_bf16_diag", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
     "KERNELS", "kd_timing_start", "kd_timing_stop", "kd_timing_query", "kd_timing_release",
 ]
@@ -77,6 +78,12 @@ def lib() -> ctypes.CDLL:
                                                   f32, ctypes.c_uint32, vp, vp, vp, vp, vp, vp,
                                                   sz, vp, vp]
         L.kd_topk_kl_forward_backward.restype = ctypes.c_int
+        L.kd_topk_kl_forward_residual.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, f32,
+                                                  i64, vp, vp, vp, vp, vp, sz, vp, vp]
+        L.kd_topk_kl_forward_residual.restype = ctypes.c_int
+        L.kd_topk_kl_backward_residual.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, f32,
+                                                   i64, vp, vp, f32, vp, vp, vp, sz, vp, vp]
+        L.kd_topk_kl_backward_residual.restype = ctypes.c_int
         L.kd_entropy_filter_workspace_size.argtypes = [i64, ctypes.POINTER(sz)]
         L.kd_entropy_filter_workspace_size.restype = ctypes.c_int
         L.kd_entropy_filter.argtypes = [vp, vp, i64, i32, f32, i32, i32, vp, vp, vp, sz, vp, vp]
@@ -192,6 +199,34 @@ def kd_topk_kl_forward_backward(h, W, teacher_idx, teacher_logits, valid, tau, c
         _ptr(dh), _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
         _stream(stream))
     _check(rc, "kd_topk_kl_forward_backward")
+
+
+def kd_topk_kl_forward_residual(h, W, teacher_idx, teacher_logits, teacher_lse, valid, tau, chunk,
+                                loss, lse, row_kl=None, topk_mass=None, *, ws, dev_status,
+                                stream=None):
+    """Forward of the residual-mass variant (teacher full-vocabulary normaliser)."""
+    T, d = h.shape
+    V = W.shape[0]
+    K = teacher_idx.shape[1]
+    rc = lib().kd_topk_kl_forward_residual(
+        _ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits), _ptr(teacher_lse), _ptr(valid),
+        T, V, d, K, float(tau), int(chunk), _ptr(loss), _ptr(lse), _ptr(row_kl), _ptr(topk_mass),
+        _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    _check(rc, "kd_topk_kl_forward_residual")
+
+
+def kd_topk_kl_backward_residual(h, W, teacher_idx, teacher_logits, teacher_lse, valid, tau,
+                                 chunk, lse, topk_mass, grad_loss, dh, dW, *, ws, dev_status,
+                                 stream=None):
+    """Backward of the residual-mass variant; lse and topk_mass from its forward."""
+    T, d = h.shape
+    V = W.shape[0]
+    K = teacher_idx.shape[1]
+    rc = lib().kd_topk_kl_backward_residual(
+        _ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits), _ptr(teacher_lse), _ptr(valid),
+        T, V, d, K, float(tau), int(chunk), _ptr(lse), _ptr(topk_mass), float(grad_loss), _ptr(dh),
+        _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    _check(rc, "kd_topk_kl_backward_residual")
 
 
 def kd_entropy_filter_workspace_size(T: int) -> int:

@@ -103,7 +103,7 @@ int dh_max_splits(int64_t V) {
 }
 
 struct Layout {
-  size_t nvalid, losspart, sidx, sp, sslot, tterm;  // shared by both passes
+  size_t nvalid, losspart, sidx, sp, sslot, tterm, resid;  // shared by both passes
   size_t zg, part;                                  // forward
   size_t rowmap, split_info, hc, dz, dhpart;        // backward
   size_t fwd_total, bwd_total;
@@ -121,6 +121,7 @@ Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
   L.sp = off;       off += al256(static_cast<size_t>(T * K) * 4);
   L.sslot = off;    off += al256(static_cast<size_t>(T * K) * 2);
   L.tterm = off;    off += al256(static_cast<size_t>(T) * 4);
+  L.resid = off;    off += al256(static_cast<size_t>(T) * 4);
   const size_t common = off;
   L.zg = off;       off += al256(static_cast<size_t>(T * K) * 4);
   L.part = off;     off += al256(static_cast<size_t>(cdiv(V, ZBN) * T) * 4);
@@ -245,23 +246,38 @@ struct Ws {
   float* sp;
   int16_t* sslot;
   float* tterm;
+  float* resid;
 };
 
 Ws carve(void* ws, const Layout& L) {
   char* w = static_cast<char*>(ws);
   return Ws{reinterpret_cast<int*>(w + L.nvalid), reinterpret_cast<double*>(w + L.losspart),
             reinterpret_cast<int*>(w + L.sidx),   reinterpret_cast<float*>(w + L.sp),
-            reinterpret_cast<int16_t*>(w + L.sslot), reinterpret_cast<float*>(w + L.tterm)};
+            reinterpret_cast<int16_t*>(w + L.sslot), reinterpret_cast<float*>(w + L.tterm),
+            reinterpret_cast<float*>(w + L.resid)};
 }
 
+// Normalisation of the teacher's cached entries.  Main loss: all pointers null
+// (softmax renormalised over the K entries).  Residual variant: teacher_lse is
+// the teacher's full-vocabulary log-normaliser at tau; the forward writes the
+// student's mass on the cached entries to topk_mass_out and the backward reads
+// it back from topk_mass_in.
+struct Variant {
+  const float* teacher_lse = nullptr;
+  float* topk_mass_out = nullptr;
+  const float* topk_mass_in = nullptr;
+  bool residual() const { return teacher_lse != nullptr; }
+};
+
 int run_prep(const int32_t* idx, const float* tl, const uint8_t* valid, int64_t T, int32_t K,
-             int64_t V, float inv_tau, const Ws& w, int32_t* dev_status, cudaStream_t st) {
+             int64_t V, float inv_tau, const Ws& w, const Variant& var, int32_t* dev_status,
+             cudaStream_t st) {
   if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
   if (cudaMemsetAsync(w.nvalid, 0, sizeof(int), st) != cudaSuccess) return KD_ERR_CUDA;
   const int rows_per_block = 8;
   kd_prep_kernel<<<static_cast<unsigned>(cdiv(T, rows_per_block)), 32 * rows_per_block, 0, st>>>(
-      idx, tl, valid, static_cast<int>(T), K, static_cast<int>(V), inv_tau, w.sidx, w.sp, w.sslot,
-      w.tterm, w.nvalid, dev_status);
+      idx, tl, var.teacher_lse, valid, static_cast<int>(T), K, static_cast<int>(V), inv_tau, w.sidx,
+      w.sp, w.sslot, w.tterm, var.residual() ? w.resid : nullptr, w.nvalid, dev_status);
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
@@ -365,8 +381,8 @@ namespace {
 // gather epilogue, combine, loss.  lse may be null (loss-only evaluation).
 int enqueue_forward(const void* h, const void* W, const uint8_t* valid, int64_t T, int64_t V,
                     int64_t d, int32_t K, float tau, const Layout& L, void* ws, const Ws& w,
-                    int sms, float* loss, float* lse, float* row_kl, int32_t* gathered_idx,
-                    int32_t* dev_status, cudaStream_t st) {
+                    const Variant& var, int sms, float* loss, float* lse, float* row_kl,
+                    int32_t* gathered_idx, int32_t* dev_status, cudaStream_t st) {
   int rc = KD_OK;
   char* wb = static_cast<char*>(ws);
   float* zg = reinterpret_cast<float*>(wb + L.zg);
@@ -392,7 +408,8 @@ int enqueue_forward(const void* h, const void* W, const uint8_t* valid, int64_t 
 
   const int nb = static_cast<int>(cdiv(T, 256));
   kd_combine_kernel<<<nb, 256, 0, st>>>(part, p.n_tiles, static_cast<int>(T), K, w.sp, zg,
-                                        w.tterm, valid, lse, row_kl, w.losspart);
+                                        w.tterm, var.residual() ? w.resid : nullptr, valid, lse,
+                                        row_kl, var.topk_mass_out, w.losspart);
   kd_loss_final_kernel<<<1, 256, 0, st>>>(w.losspart, nb, w.nvalid, loss);
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
@@ -403,8 +420,8 @@ int enqueue_forward(const void* h, const void* W, const uint8_t* valid, int64_t 
 // overwriting it.
 int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t T, int64_t V,
                      int64_t d, int32_t K, float tau, const Layout& L, void* ws, const Ws& w,
-                     int sms, const float* lse, float grad_loss, float* dh, float* dW,
-                     int accumulate_dW, int32_t* dev_status, cudaStream_t st) {
+                     const Variant& var, int sms, const float* lse, float grad_loss, float* dh,
+                     float* dW, int accumulate_dW, int32_t* dev_status, cudaStream_t st) {
   int rc = KD_OK;
   char* wb = static_cast<char*>(ws);
   int* rowmap = reinterpret_cast<int*>(wb + L.rowmap);
@@ -446,6 +463,8 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
     p.inv_tau = inv_tau;
     p.c_log2 = LOG2E * inv_tau;
     p.lse = lse;
+    p.resid = var.residual() ? w.resid : nullptr;
+    p.topk_mass = var.topk_mass_in;
     p.valid = valid;
     p.nvalid = w.nvalid;
     p.grad_loss = grad_loss;
@@ -549,9 +568,11 @@ int kd_topk_kl_forward(const void* h, const void* W, const int32_t* teacher_idx,
   if (!encode_fn()) return KD_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const Ws w = carve(ws, L);
-  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, dev_status, st)))
+  const Variant var;
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
+                     st)))
     return rc;
-  return enqueue_forward(h, W, valid, T, V, d, K, tau, L, ws, w, sms, loss, lse, row_kl,
+  return enqueue_forward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, loss, lse, row_kl,
                          gathered_idx, dev_status, st);
 }
 
@@ -572,10 +593,12 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
   if (!encode_fn()) return KD_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const Ws w = carve(ws, L);
-  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, dev_status, st)))
+  const Variant var;
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
+                     st)))
     return rc;
-  return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, sms, lse, grad_loss, dh, dW, 0,
-                          dev_status, st);
+  return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, lse, grad_loss, dh, dW,
+                          0, dev_status, st);
 }
 
 int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* teacher_idx,
@@ -599,12 +622,14 @@ int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* tea
   const Ws w = carve(ws, L);
   // one teacher prep serves both passes: the backward's buffers overlay the
   // forward's lse partials, which the combine has consumed by then
-  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, dev_status, st)))
+  const Variant var;
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
+                     st)))
     return rc;
-  if ((rc = enqueue_forward(h, W, valid, T, V, d, K, tau, L, ws, w, sms, loss, lse, row_kl,
+  if ((rc = enqueue_forward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, loss, lse, row_kl,
                             nullptr, dev_status, st)))
     return rc;
-  return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, sms, lse, grad_loss, dh, dW,
+  return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, lse, grad_loss, dh, dW,
                           (flags & KD_ACCUMULATE_DW) ? 1 : 0, dev_status, st);
 }
 
@@ -732,6 +757,66 @@ int kd_timing_release(void) {
   t.recording = false;
   destroy_timing_events(t);
   return KD_OK;
+}
+
+int kd_topk_kl_forward_residual(const void* h, const void* W, const int32_t* teacher_idx,
+                                const float* teacher_logits, const float* teacher_lse,
+                                const uint8_t* valid, int64_t T, int64_t V, int64_t d, int32_t K,
+                                float tau, int64_t chunk, float* loss, float* lse, float* row_kl,
+                                float* topk_mass, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                struct CUstream_st* stream) {
+  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
+                        dev_status);
+  if (rc != KD_OK) return rc;
+  if (!loss || !teacher_lse || (reinterpret_cast<uintptr_t>(teacher_lse) & 3u))
+    return KD_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, V, d, K, chunk);
+  if (ws_bytes < L.fwd_total) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Ws w = carve(ws, L);
+  Variant var;
+  var.teacher_lse = teacher_lse;
+  var.topk_mass_out = topk_mass;
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
+                     st)))
+    return rc;
+  return enqueue_forward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, loss, lse, row_kl,
+                         nullptr, dev_status, st);
+}
+
+int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* teacher_idx,
+                                 const float* teacher_logits, const float* teacher_lse,
+                                 const uint8_t* valid, int64_t T, int64_t V, int64_t d, int32_t K,
+                                 float tau, int64_t chunk, const float* lse,
+                                 const float* topk_mass, float grad_loss, float* dh, float* dW,
+                                 void* ws, size_t ws_bytes, int32_t* dev_status,
+                                 struct CUstream_st* stream) {
+  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
+                        dev_status);
+  if (rc != KD_OK) return rc;
+  if (!lse || !topk_mass || !teacher_lse || !dh || !dW || !aligned16(dh) || !aligned16(dW) ||
+      (reinterpret_cast<uintptr_t>(teacher_lse) & 3u) ||
+      (reinterpret_cast<uintptr_t>(topk_mass) & 3u))
+    return KD_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_loss)) return KD_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, V, d, K, chunk);
+  if (ws_bytes < L.bwd_total) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Ws w = carve(ws, L);
+  Variant var;
+  var.teacher_lse = teacher_lse;
+  var.topk_mass_in = topk_mass;
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
+                     st)))
+    return rc;
+  return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, lse, grad_loss, dh, dW,
+                          0, dev_status, st);
 }
 
 int kd_entropy_filter_workspace_size(int64_t T, size_t* bytes) {

@@ -78,6 +78,8 @@ struct GemmParams {
   float* zg;              // [T][K] z / tau gathered at the sorted entries
   int* gidx;              // [T][K] (slot order) vocabulary column read, or null
   const float* lse;       // [T]
+  const float* resid;     // [T] teacher mass outside the cached entries, or null (main loss)
+  const float* topk_mass; // [T] student mass on the cached entries (with resid)
   const uint8_t* valid;   // [T]
   const int* nvalid;      // device scalar
   float grad_loss;
@@ -367,6 +369,7 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
   const int* srow = p.sidx + grow * p.K;
   float sc = 0.f;   // g * valid / N_valid / tau
   float lb = 0.f;   // lse in base 2
+  float rq = 0.f;   // residual variant: R / Q (0 for the main loss)
   int pos = p.K;
   int nxt = INT_MAX;
   if (active) {
@@ -374,10 +377,16 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
     if (p.valid[grow] && nv > 0) {
       sc = p.grad_loss / static_cast<float>(nv) * p.inv_tau;
       lb = p.lse[grow] * LOG2E;
+      if (p.resid) {
+        const float R = p.resid[grow];
+        if (R > 0.f) rq = R / (1.f - p.topk_mass[grow]);
+      }
       pos = lower_bound_row(srow, p.K, v0);
       nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
     }
   }
+  // every column gets a q (1 - R/Q); each cached slot adds (R/Q) q - P
+  const float a_row = sc * (1.f - rq);
   bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
   ok = __all_sync(0xffffffffu, w);
   if (!ok) return;
@@ -393,7 +402,7 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
     float g[32];
     if (sc != 0.f) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) g[j] = sc * ex2f(__uint_as_float(r[j]) * p.c_log2 - lb);
+      for (int j = 0; j < 32; ++j) g[j] = a_row * ex2f(__uint_as_float(r[j]) * p.c_log2 - lb);
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j) g[j] = 0.f;
@@ -402,9 +411,15 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
     while (__any_sync(0xffffffffu, nxt < ce)) {
       if (nxt < ce) {
         const int j = nxt - cb;
-        const float dp = sc * __ldg(p.sp + grow * p.K + pos);
+        float add = -(sc * __ldg(p.sp + grow * p.K + pos));
+        if (rq != 0.f) {
+          uint32_t bits = 0;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) g[jj] = (jj == j) ? g[jj] - dp : g[jj];
+          for (int jj = 0; jj < 32; ++jj) bits = (jj == j) ? r[jj] : bits;
+          add += sc * rq * ex2f(__uint_as_float(bits) * p.c_log2 - lb);
+        }
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) g[jj] = (jj == j) ? g[jj] + add : g[jj];
         ++pos;
         nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
       }
@@ -705,14 +720,18 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Teacher side of each row, one warp per row: range check of the cached
-// indices, p = softmax(teacher_logits / tau) over the K entries, the teacher
-// term sum_k p log p, and the entries sorted by vocabulary index (ties keep
-// slot order) so that the contraction epilogues can walk them tile by tile.
+// indices, the teacher probabilities of the K entries, the teacher term
+// sum_k p log p, and the entries sorted by vocabulary index (ties keep slot
+// order) so that the contraction epilogues can walk them tile by tile.
+// teacher_lse == null: p = softmax(teacher_logits / tau) over the K entries
+// (renormalised).  Otherwise p = exp(teacher_logits / tau - teacher_lse) under
+// the teacher's full-vocabulary normaliser and resid = max(0, 1 - sum_k p).
 __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restrict__ tl,
+                               const float* __restrict__ teacher_lse,
                                const uint8_t* __restrict__ valid, int T, int K, int V,
                                float inv_tau, int* __restrict__ sidx, float* __restrict__ sp,
                                int16_t* __restrict__ sslot, float* __restrict__ tterm,
-                               int* __restrict__ nvalid, int* status) {
+                               float* __restrict__ resid, int* __restrict__ nvalid, int* status) {
   const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= T) return;
@@ -727,18 +746,26 @@ __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restr
   }
   m = warp_max(m);
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, KD_ERR_INDEX_RANGE);
-  float S = 0.f;
-  for (int k = lane; k < K; k += 32) S += expf(tr[k] * inv_tau - m);
-  S = warp_sum(S);
-  const float logS = logf(S);
+  float L = 0.f;     // full-vocabulary normaliser (teacher_lse given)
+  float logS = 0.f;  // log sum_k exp(a_k - m) (renormalised top-K)
+  if (teacher_lse) {
+    L = teacher_lse[row];
+  } else {
+    float S = 0.f;
+    for (int k = lane; k < K; k += 32) S += expf(tr[k] * inv_tau - m);
+    S = warp_sum(S);
+    logS = logf(S);
+  }
   float tt = 0.f;
+  float psum = 0.f;
   int* so = sidx + static_cast<int64_t>(row) * K;
   float* po = sp + static_cast<int64_t>(row) * K;
   int16_t* lo = sslot + static_cast<int64_t>(row) * K;
   for (int k = lane; k < K; k += 32) {
-    const float lp = tr[k] * inv_tau - m - logS;
+    const float lp = teacher_lse ? tr[k] * inv_tau - L : tr[k] * inv_tau - m - logS;
     const float pk = expf(lp);
     if (pk > 0.f) tt += pk * lp;
+    psum += pk;
     const int v = ir[k];
     int rank = 0;
     for (int j = 0; j < K; ++j) {
@@ -750,19 +777,27 @@ __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restr
     lo[rank] = static_cast<int16_t>(k);
   }
   tt = warp_sum(tt);
+  psum = warp_sum(psum);
   if (lane == 0) {
     tterm[row] = tt;
+    if (resid) resid[row] = teacher_lse ? fmaxf(0.f, 1.f - psum) : 0.f;
     if (valid[row]) atomicAdd(nvalid, 1);
   }
 }
 
 // One thread per row: lse from the per-tile partials, row_kl, and a per-block
 // (double) partial sum of row_kl for the deterministic loss reduction.
+// resid != null (residual variant): the student mass on the cached entries,
+// s = sum_k exp(zg_k - lse), goes to topk_mass_out (if given) and row_kl gains
+// R (log R - log(1 - s)) for R > 0.
 __global__ void kd_combine_kernel(const float* __restrict__ part, int n_tiles, int T, int K,
                                   const float* __restrict__ sp, const float* __restrict__ zg,
                                   const float* __restrict__ tterm,
+                                  const float* __restrict__ resid,
                                   const uint8_t* __restrict__ valid, float* __restrict__ lse_out,
-                                  float* __restrict__ row_kl_out, double* __restrict__ losspart) {
+                                  float* __restrict__ row_kl_out,
+                                  float* __restrict__ topk_mass_out,
+                                  double* __restrict__ losspart) {
   __shared__ double red[256];
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
   double kl = 0.0;
@@ -780,13 +815,22 @@ __global__ void kd_combine_kernel(const float* __restrict__ part, int n_tiles, i
     }
     const float lse = m + logf(s);
     if (lse_out) lse_out[row] = lse;
+    const float* pr = sp + static_cast<int64_t>(row) * K;
+    const float* zr = zg + static_cast<int64_t>(row) * K;
+    float mass = 0.f;
+    if (resid) {
+      for (int k = 0; k < K; ++k) mass += expf(zr[k] - lse);
+      if (topk_mass_out) topk_mass_out[row] = mass;
+    }
     float rk = 0.f;
     if (valid[row]) {
-      const float* pr = sp + static_cast<int64_t>(row) * K;
-      const float* zr = zg + static_cast<int64_t>(row) * K;
       float a = 0.f;
       for (int k = 0; k < K; ++k) a += pr[k] * (lse - zr[k]);
       rk = tterm[row] + a;
+      if (resid) {
+        const float R = resid[row];
+        if (R > 0.f) rk += R * (logf(R) - log1pf(-mass));
+      }
     }
     if (row_kl_out) row_kl_out[row] = rk;
     kl = rk;

@@ -156,6 +156,45 @@ int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* tea
                                 int32_t* dev_status, struct CUstream_st* stream);
 
 /*
+ * Residual-mass variant.  The pages cache only the teacher's top-100 logits per
+ * position (aipuls.nl summary, section "Summary") and leave open what happens
+ * to the probability mass outside them.  kd_topk_kl_forward renormalises the
+ * teacher over the K entries; this variant instead takes the teacher's
+ * full-vocabulary log-normaliser at temperature tau, cached beside the top-K,
+ *
+ *   teacher_lse_t = log sum_v exp(teacher_logit_tv / tau)   (fp32 [T], device),
+ *
+ * and compares teacher and student over K + 1 outcomes: the K cached entries
+ * and "everything else".
+ *
+ *   P_tk = exp(teacher_logits_tk / tau - teacher_lse_t),  R_t = 1 - sum_k P_tk
+ *   q_tk = exp(z_t,idx_tk / tau - lse_t),                 Q_t = 1 - sum_k q_tk
+ *   row_kl_t = sum_k P_tk (log P_tk - log q_tk) + R_t (log R_t - log Q_t)
+ *              (the last term is 0 when R_t = 0; R_t is clamped at 0)
+ *   G_tv = s_t / tau (q_tv (1 - R_t/Q_t) + (R_t/Q_t) c_tv q_tv - sum_{k: idx_tk = v} P_tk)
+ *   with s_t = grad_loss valid_t / N_valid and c_tv the number of slots holding v.
+ *
+ * The forward also writes topk_mass_t = sum_k q_tk (fp32 [T], device, or
+ * NULL); the backward needs it (with lse) from the forward.  Other arguments,
+ * outputs, workspace sizes and errors as kd_topk_kl_forward / _backward.  A row
+ * whose student puts all its mass on the cached entries (Q_t = 0) while
+ * R_t > 0 has an infinite loss, as the definition says.
+ */
+int kd_topk_kl_forward_residual(const void* h, const void* W, const int32_t* teacher_idx,
+                                const float* teacher_logits, const float* teacher_lse,
+                                const uint8_t* valid, int64_t T, int64_t V, int64_t d, int32_t K,
+                                float tau, int64_t chunk, float* loss, float* lse, float* row_kl,
+                                float* topk_mass, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                struct CUstream_st* stream);
+int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* teacher_idx,
+                                 const float* teacher_logits, const float* teacher_lse,
+                                 const uint8_t* valid, int64_t T, int64_t V, int64_t d, int32_t K,
+                                 float tau, int64_t chunk, const float* lse,
+                                 const float* topk_mass, float grad_loss, float* dh, float* dW,
+                                 void* ws, size_t ws_bytes, int32_t* dev_status,
+                                 struct CUstream_st* stream);
+
+/*
  * Teacher-entropy token filter, the producer of the valid mask (asibiont.com
  * rewrite, section "Distillation Token Filtering": score each token by the
  * entropy of the teacher's distribution and keep, per batch, a fixed

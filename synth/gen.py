@@ -26,7 +26,7 @@ import dataclasses
 import numpy as np
 import torch
 
-__all__ = ["Workload", "WORKLOADS", "make_inputs", "workload"]
+__all__ = ["Workload", "WORKLOADS", "make_inputs", "workload", "teacher_full_lse"]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -186,3 +186,18 @@ def make_inputs(w: Workload, seed: int = 0, device=None) -> dict:
         "tau": float(w.tau),
         "workload": w,
     }
+
+
+def teacher_full_lse(teacher_logits: torch.Tensor, tau: float, seed: int = 0,
+                     lo: float = 0.05, hi: float = 0.5) -> torch.Tensor:
+    """Full-vocabulary log-normaliser of a synthetic teacher, for the
+    residual-mass variant of the loss: per row a share r ~ U(lo, hi) of the
+    teacher's probability mass (at temperature tau) lies outside its cached
+    entries, so L = logsumexp(teacher_logits / tau) - log(1 - r).  fp32 [T].
+    Draws from its own generator (seed), after the other inputs."""
+    rng = np.random.default_rng(seed + 7919)
+    a = teacher_logits.double().numpy() / float(tau)
+    m = a.max(axis=1)
+    lse_k = m + np.log(np.exp(a - m[:, None]).sum(axis=1))
+    r = rng.uniform(lo, hi, size=a.shape[0])
+    return torch.from_numpy((lse_k - np.log1p(-r)).astype(np.float32))

@@ -154,3 +154,24 @@ def test_forward_backward_argument_checks():
     assert L.kd_topk_kl_forward_backward(*args(2, A, max(f, b))) == INVALID
     assert L.kd_topk_kl_forward_backward(*args(0, None, max(f, b))) == INVALID
     assert L.kd_topk_kl_forward_backward(*args(0, A, min(f, b) - 1)) == WORKSPACE
+
+
+def test_residual_entry_argument_checks():
+    """The residual-mass entries need teacher_lse (and the backward topk_mass)
+    and reject their absence before any CUDA call."""
+    vp = ctypes.c_void_p
+    L = kd.lib()
+    T, V, d, K, chunk = 16, 1024, 64, 4, 16
+    f, b = kd.kd_topk_kl_workspace_size(T, V, d, K, chunk)
+    assert L.kd_topk_kl_forward_residual(vp(A), vp(A), vp(A), vp(A), None, vp(A), T, V, d, K, 1.0,
+                                         chunk, vp(A), vp(A), None, None, vp(A), f, vp(A),
+                                         None) == INVALID
+    assert L.kd_topk_kl_forward_residual(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), T, V, d, K,
+                                         1.0, chunk, vp(A), vp(A), None, None, vp(A), f - 1,
+                                         vp(A), None) == WORKSPACE
+    assert L.kd_topk_kl_backward_residual(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), T, V, d, K,
+                                          1.0, chunk, vp(A), None, 1.0, vp(A), vp(A), vp(A), b,
+                                          vp(A), None) == INVALID
+    assert L.kd_topk_kl_backward_residual(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), T, V, d, K,
+                                          1.0, chunk, vp(A), vp(A), 1.0, vp(A), vp(A), vp(A),
+                                          b - 1, vp(A), None) == WORKSPACE

@@ -1,0 +1,121 @@
+"""The residual-mass variant (kd_topk_kl_forward_residual / _backward_residual)
+through the C ABI against its fp64 oracle, with the project's tolerances, on
+seeded inputs spanning several tiles with ragged tails; plus the special case
+with no residual mass, which must agree with the main loss."""
+
+import numpy as np
+import pytest
+import torch
+
+import chunked_top_kl_logit_b300 as kd
+from oracle import kd_oracle as O
+from oracle import kd_residual_oracle as RO
+from synth import make_inputs, teacher_full_lse, workload
+from tests.gpu_util import GRAD_RL2, LOSS_RTOL, LSE_ATOL, oracle_inputs, rel_l2, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+MASS_ATOL = 1e-4
+
+
+def run_gpu_resid(x, tlse, chunk, grad_loss=1.0, backward=True):
+    g = to_device(x)
+    T, d = g["h"].shape
+    V, K = g["W"].shape[0], g["teacher_idx"].shape[1]
+    dev = torch.device("cuda")
+    fwd, bwd = kd.kd_topk_kl_workspace_size(T, V, d, K, chunk)
+    ws = torch.empty(max(fwd, bwd), dtype=torch.uint8, device=dev)
+    st = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    loss = torch.empty(1, device=dev)
+    lse = torch.empty(T, device=dev)
+    row_kl = torch.empty(T, device=dev)
+    mass = torch.empty(T, device=dev)
+    tl_d = tlse.to(dev).contiguous()
+    kd.kd_topk_kl_forward_residual(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], tl_d,
+                                   g["valid"], g["tau"], chunk, loss, lse, row_kl, mass, ws=ws,
+                                   dev_status=st)
+    torch.cuda.synchronize()
+    out = dict(fwd_status=int(st.item()), loss=float(loss.item()), lse=lse.double().cpu().numpy(),
+               row_kl=row_kl.double().cpu().numpy(), topk_mass=mass.double().cpu().numpy())
+    if backward:
+        dh = torch.empty(T, d, device=dev)
+        dW = torch.empty(V, d, device=dev)
+        kd.kd_topk_kl_backward_residual(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"],
+                                        tl_d, g["valid"], g["tau"], chunk, lse, mass, grad_loss,
+                                        dh, dW, ws=ws, dev_status=st)
+        torch.cuda.synchronize()
+        out.update(bwd_status=int(st.item()), dh=dh.double().cpu().numpy(),
+                   dW=dW.double().cpu().numpy())
+    return out
+
+
+CASES = [
+    ("teacher_T300_V5000_d256", dict(T=300, d=256, V=5000, tau=1.0), 128),
+    ("packed_T520_V3000_d320_tau2", dict(T=520, d=320, V=3000, K=64, tau=2.0, mask_kind="packed",
+                                         seq_len=130, pad=30), 200),
+    ("uniform_T1000_V8192_d384", dict(T=1000, d=384, V=8192, K=100, tau=1.5, idx_kind="uniform"),
+     512),
+]
+
+
+@pytest.mark.parametrize("name,over,chunk", CASES, ids=[c[0] for c in CASES])
+def test_residual_parity(name, over, chunk):
+    x = make_inputs(workload("small_4k", **over))
+    tlse = teacher_full_lse(x["teacher_logits"], x["tau"])
+    gpu = run_gpu_resid(x, tlse, chunk, grad_loss=0.8)
+    assert gpu["fwd_status"] == 0 and gpu["bwd_status"] == 0
+    P = oracle_inputs(x)
+    tl64 = tlse.double().numpy()
+    args = (P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tl64, P["valid"], P["tau"])
+    f = RO.forward(*args)
+    dh, dW = RO.backward(*args, 0.8, f["lse"], f["topk_mass"])
+    assert abs(gpu["loss"] - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert np.abs(gpu["lse"] - f["lse"]).max() <= LSE_ATOL
+    assert np.abs(gpu["row_kl"] - f["row_kl"]).max() <= LSE_ATOL
+    assert np.abs(gpu["topk_mass"] - f["topk_mass"]).max() <= MASS_ATOL
+    assert rel_l2(gpu["dh"], dh) <= GRAD_RL2
+    assert rel_l2(gpu["dW"], dW) <= GRAD_RL2
+    assert np.all(gpu["dh"][P["valid"] == 0] == 0.0)
+
+
+def test_no_residual_mass_matches_main_loss():
+    """teacher_lse = logsumexp of the cached logits: no mass outside the cache,
+    so the variant is the renormalised main loss (up to fp32 rounding of the
+    two normalisations)."""
+    x = make_inputs(workload("small_4k", T=400, d=192, V=4000, K=50, tau=1.0))
+    a = x["teacher_logits"].double() / x["tau"]
+    tlse = torch.logsumexp(a, dim=1).float()
+    res = run_gpu_resid(x, tlse, 128)
+    main = run_gpu(x, 128)
+    assert abs(res["loss"] - main["loss"]) <= LOSS_RTOL * abs(main["loss"])
+    assert np.abs(res["row_kl"] - main["row_kl"]).max() <= LSE_ATOL
+    np.testing.assert_array_equal(res["lse"], main["lse"])
+    assert rel_l2(res["dh"], main["dh"]) <= 1e-3
+    assert rel_l2(res["dW"], main["dW"]) <= 1e-3
+
+
+def test_residual_full_vocab_small_4k_sampled():
+    """T=4096, V=201088, d=2880: the oracle checks sampled rows (lse, row KL,
+    student top-K mass, dh) and dW column sums vanish."""
+    w = workload("small_4k")
+    x = make_inputs(w)
+    tlse = teacher_full_lse(x["teacher_logits"], x["tau"])
+    gpu = run_gpu_resid(x, tlse, w.chunk)
+    assert gpu["fwd_status"] == 0 and gpu["bwd_status"] == 0
+    P = oracle_inputs(x)
+    rng = np.random.default_rng(3)
+    rows = np.sort(rng.choice(w.T, 12, replace=False))
+    tl64 = tlse.double().numpy()
+    sub = dict(h=P["h"][rows], idx=P["teacher_idx"][rows], tl=P["teacher_logits"][rows],
+               tlse=tl64[rows], valid=np.ones(len(rows), dtype=np.uint8))
+    f = RO.forward(sub["h"], P["W"], sub["idx"], sub["tl"], sub["tlse"], sub["valid"], P["tau"])
+    assert np.abs(gpu["lse"][rows] - f["lse"]).max() <= LSE_ATOL
+    assert np.abs(gpu["topk_mass"][rows] - f["topk_mass"]).max() <= MASS_ATOL
+    kl = np.where(P["valid"][rows] > 0, f["row_kl"], 0.0)
+    assert np.abs(gpu["row_kl"][rows] - kl).max() <= LSE_ATOL
+    n_valid = int((P["valid"] > 0).sum())
+    G = RO.grad_logits_rows(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tl64,
+                            P["valid"], P["tau"], 1.0, gpu["lse"], gpu["topk_mass"], n_valid, rows)
+    assert rel_l2(gpu["dh"][rows], G @ P["W"]) <= GRAD_RL2
+    col = gpu["dW"].sum(axis=0)
+    assert np.linalg.norm(col) <= 1e-2 * np.linalg.norm(gpu["dW"])

@@ -497,3 +497,120 @@ def test_entropy_filter_extremes():
     assert np.array_equal(EF.entropy_filter(H, valid, 1, 3), [0, 0, 0, 1])
     # ties: rows 0 and 2 share H, row 2 is not a candidate; row 0 before row 1
     assert np.array_equal(EF.entropy_filter(H, valid, 2, 3), [1, 0, 0, 1])
+
+
+# --------------------------------------------------------------------------
+# residual-mass variant (teacher full-vocabulary normaliser cached with the
+# top-K; one extra "everything else" outcome)
+# --------------------------------------------------------------------------
+
+from oracle import kd_residual_oracle as RO  # noqa: E402
+
+
+def resid_problem(T, d, V, K, tau, seed, masked=(), r_lo=0.05, r_hi=0.5, grad_loss=1.0):
+    P = rand_problem(T, d, V, K, tau, seed, masked=masked, grad_loss=grad_loss)
+    a = P["teacher_logits"] / tau
+    r = np.random.default_rng(seed + 1).uniform(r_lo, r_hi, size=T)
+    P["teacher_lse"] = scipy.special.logsumexp(a, axis=1) - np.log1p(-r)
+    P["r"] = r
+    return P
+
+
+def run_resid(P, mod=RO):
+    f = mod.forward(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], P["teacher_lse"],
+                    P["valid"], P["tau"])
+    dh, dW = mod.backward(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"],
+                          P["teacher_lse"], P["valid"], P["tau"], P["grad_loss"], f["lse"],
+                          f["topk_mass"])
+    return f, dh, dW
+
+
+def test_residual_zero_reduces_to_main_loss():
+    """teacher_lse = logsumexp of the cached logits leaves no residual mass:
+    the variant is the renormalised loss exactly."""
+    P = rand_problem(12, 8, 40, 6, 1.5, seed=21, masked=(3,))
+    P["teacher_lse"] = scipy.special.logsumexp(P["teacher_logits"] / P["tau"], axis=1)
+    f, dh, dW = run_resid(P)
+    g, dh0, dW0 = run(P)
+    assert abs(f["loss"] - g["loss"]) < 1e-12
+    assert np.allclose(f["row_kl"], g["row_kl"], atol=1e-12)
+    assert rel(dh, dh0) < 1e-10 and rel(dW, dW0) < 1e-10
+
+
+def test_residual_bucket_kl_with_scipy():
+    """Row KL against scipy's rel_entr on the explicit K+1-outcome
+    distributions built from a full-vocabulary softmax."""
+    P = resid_problem(9, 6, 30, 5, 0.8, seed=22)
+    f, _, _ = run_resid(P)
+    z = P["h"] @ P["W"].T / P["tau"]
+    q = scipy.special.softmax(z, axis=1)
+    for t in range(9):
+        pt = np.exp(P["teacher_logits"][t] / P["tau"] - P["teacher_lse"][t])
+        qt = q[t, P["teacher_idx"][t]]
+        p_full = np.append(pt, 1.0 - pt.sum())
+        q_full = np.append(qt, 1.0 - qt.sum())
+        assert abs(p_full[-1] - P["r"][t]) < 1e-12
+        assert abs(scipy.special.rel_entr(p_full, q_full).sum() - f["row_kl"][t]) < 1e-12
+    assert np.all(f["row_kl"] >= 0)
+
+
+@pytest.mark.parametrize("tau", [1.0, 2.0])
+def test_residual_gradient_with_autograd(tau):
+    """dh and dW against torch autograd of the bucketed loss (fp64)."""
+    P = resid_problem(10, 7, 25, 4, tau, seed=23, masked=(0, 6), grad_loss=0.7)
+    f, dh, dW = run_resid(P)
+    h = torch.tensor(P["h"], requires_grad=True)
+    W = torch.tensor(P["W"], requires_grad=True)
+    idx = torch.tensor(P["teacher_idx"], dtype=torch.long)
+    logq = torch.log_softmax(h @ W.T / tau, dim=1)
+    lqk = torch.gather(logq, 1, idx)
+    pk = torch.exp(torch.tensor(P["teacher_logits"]) / tau - torch.tensor(P["teacher_lse"])[:, None])
+    R = 1.0 - pk.sum(1)
+    Q = 1.0 - torch.exp(lqk).sum(1)
+    kl = (pk * (torch.log(pk) - lqk)).sum(1) + R * (torch.log(R) - torch.log(Q))
+    valid = torch.tensor(P["valid"], dtype=torch.float64)
+    loss = (kl * valid).sum() / valid.sum()
+    (loss * P["grad_loss"]).backward()
+    assert abs(loss.item() - f["loss"]) < 1e-12
+    assert rel(dh, h.grad.numpy()) < 1e-10
+    assert rel(dW, W.grad.numpy()) < 1e-10
+
+
+def test_residual_finite_differences():
+    P = resid_problem(4, 5, 16, 3, 1.3, seed=24, masked=(2,))
+    f, dh, dW = run_resid(P)
+    eps = 1e-6
+    for (M, G) in ((P["h"], dh), (P["W"], dW)):
+        for i in range(M.shape[0]):
+            for j in range(M.shape[1]):
+                old = M[i, j]
+                M[i, j] = old + eps
+                lp = RO.forward(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"],
+                                P["teacher_lse"], P["valid"], P["tau"])["loss"]
+                M[i, j] = old - eps
+                lm = RO.forward(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"],
+                                P["teacher_lse"], P["valid"], P["tau"])["loss"]
+                M[i, j] = old
+                assert abs((lp - lm) / (2 * eps) - G[i, j]) < 1e-7
+
+
+def test_residual_gradient_rows_sum_to_zero():
+    P = resid_problem(8, 6, 50, 7, 1.0, seed=25)
+    f = RO.forward(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], P["teacher_lse"],
+                   P["valid"], P["tau"])
+    G = RO.grad_logits_rows(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"],
+                            P["teacher_lse"], P["valid"], P["tau"], 1.0, f["lse"],
+                            f["topk_mass"], f["n_valid"], np.arange(8))
+    assert np.abs(G.sum(axis=1)).max() < 1e-15
+
+
+def test_planted_residual_gradient_without_bucket_term(monkeypatch):
+    """Dropping the R/Q terms of the gradient is caught by the autograd pin."""
+    orig = RO.grad_logits_rows
+
+    def broken(h, W, idx, tl, tlse, valid, tau, g, lse, tm, nv, rows):
+        z = np.zeros_like(np.asarray(tm))
+        return orig(h, W, idx, tl, tlse, valid, tau, g, lse, np.full_like(z, -np.inf), nv, rows)
+    monkeypatch.setattr(RO, "grad_logits_rows", broken)
+    with pytest.raises(AssertionError):
+        test_residual_gradient_with_autograd(1.0)
