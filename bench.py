@@ -423,6 +423,81 @@ def run_ours(args, w, world, rank, local_rank):
     return out
 
 
+def run_teacher_topk(args, w, world, rank, local_rank):
+    """The teacher-side top-K cache producer on the workload's shape (h, W of a
+    synthetic teacher): one step = one kd_teacher_topk call over all T rows
+    (two logit passes per row chunk + selection).  Roofline: tensor, 2 d V
+    FLOPs per row per pass, for the dominant pass (from the library's launch
+    events)."""
+    import chunked_top_kl_logit_b300 as kd
+    from synth import make_inputs
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    x = make_inputs(w.replace(idx_kind="uniform"), seed=args.seed + rank, device=dev)
+    h, W = x["h"].to(dev), x["W"].to(dev)
+    T, d, V, K = w.T, w.d, w.V, w.K
+    chunk = args.chunk or 4096
+    ws = torch.empty(kd.kd_teacher_topk_workspace_size(T, V, d, K, chunk), dtype=torch.uint8,
+                     device=dev)
+    idx = torch.empty(T, K, dtype=torch.int32, device=dev)
+    val = torch.empty(T, K, dtype=torch.float32, device=dev)
+    lse = torch.empty(T, dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        kd.kd_teacher_topk(h, W, K, w.tau, chunk, idx, val, lse, ws=ws, dev_status=st)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    kd.check_device_status(st, "teacher_topk warm-up")
+    n = args.steps
+    chunks = (T + chunk - 1) // chunk
+    sampler = ClockSampler(None).start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    kd.kd_timing_start(2 * chunks * n + 4)
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    kd.kd_timing_stop()
+    barrier(world)
+    clocks = sampler.stop()
+    kd.check_device_status(st, "teacher_topk")
+    passes = {name: kd.kd_timing_query(kid) for name, kid in kd.PRODUCER_KERNELS.items()}
+    kd.kd_timing_release()
+    ms = e0.elapsed_time(e1)
+    max_sec = max_over_ranks(ms / 1e3, world, device=dev)
+    peaks, src = load_peaks()
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    kern = {}
+    for name, (cnt, kms) in passes.items():
+        fl = 2.0 * T * d * V * n
+        kern[name] = {"launches": cnt, "ms_per_step": kms / n,
+                      "tflops": fl / (kms / 1e3) / 1e12 if kms > 0 else None}
+    dom = max(kern, key=lambda k: kern[k]["ms_per_step"])
+    return {
+        "metric": "teacher top-K cache producer rows/s", "op": "teacher_topk",
+        "value": job_throughput(T * n, world, max_sec), "unit": "rows/s", "n_gpus": world,
+        "steps": n, "warmup": args.warmup, "ms_per_step": max_sec * 1e3 / n,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": T, "V": V, "d": d, "K": K, "tau": w.tau,
+                   "chunk": chunk, "l2": "inputs larger than L2 (W alone is V*d*2 B)"},
+        "tflops_two_passes": 4.0 * T * d * V / (max_sec / n) / 1e12,
+        "kernels": kern,
+        "roofline": {"kernel": f"kd_gemm_kernel<{kd.PRODUCER_KERNELS[dom]}> ({dom})",
+                     "bound": "tensor", "achieved": kern[dom]["tflops"], "peak": sustained,
+                     "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / sustained,
+                     "peak_kind": f"bf16 sustained, {src}", "traffic": None},
+        "clocks": clocks,
+        "gpu_launches": 4 * chunks * n,
+    }
+
+
 def run_entropy_filter(args, w, world, rank, local_rank):
     """The teacher-entropy token filter on the workload's teacher cache: one
     step = one kd_entropy_filter call (entropy of every row + exact selection),
@@ -491,9 +566,10 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
-    ap.add_argument("--op", default="loss", choices=["loss", "entropy_filter"],
+    ap.add_argument("--op", default="loss", choices=["loss", "entropy_filter", "teacher_topk"],
                     help="loss: the fused top-K KL forward + backward (headline); "
-                         "entropy_filter: the mask producer alone")
+                         "entropy_filter: the mask producer alone; "
+                         "teacher_topk: the teacher-side top-K cache producer")
     ap.add_argument("--variant", default="main", choices=["main", "residual"],
                     help="main: teacher renormalised over its top-K; residual: the teacher's "
                          "full-vocabulary normaliser and an 'everything else' outcome")
@@ -516,8 +592,9 @@ def main(argv=None):
         return 0
 
     dist_setup(world, "nccl")
-    if args.op == "entropy_filter":
-        out = run_entropy_filter(args, w, world, rank, local_rank)
+    if args.op in ("entropy_filter", "teacher_topk"):
+        run = run_entropy_filter if args.op == "entropy_filter" else run_teacher_topk
+        out = run(args, w, world, rank, local_rank)
         if rank == 0:
             print(json.dumps(out), flush=True)
         if world > 1:

@@ -31,12 +31,14 @@ __all__ = [
     "kd_topk_kl_forward_noalloc", "kd_topk_kl_backward", "kd_topk_kl_forward_backward",
     "KD_ACCUMULATE_DW", "kd_entropy_filter_workspace_size", "kd_entropy_filter",
     "kd_topk_kl_forward_residual", "kd_topk_kl_backward_residual",
+    "kd_teacher_topk_workspace_size", "kd_teacher_topk", "PRODUCER_KERNELS",
     "kd_gemm_bf16_diag", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
     "KERNELS", "kd_timing_start", "kd_timing_stop", "kd_timing_query", "kd_timing_release",
 ]
 
 # contraction kernel ids of the diagnostic timing interface
 KERNELS = {"logits_fwd": 0, "logits_bwd": 1, "dh": 3, "dW": 4}
+PRODUCER_KERNELS = {"topk_pass1": 5, "topk_pass2": 6}
 
 KD_OK = 0
 KD_ACCUMULATE_DW = 1
@@ -84,6 +86,11 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_backward_residual.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, f32,
                                                    i64, vp, vp, f32, vp, vp, vp, sz, vp, vp]
         L.kd_topk_kl_backward_residual.restype = ctypes.c_int
+        L.kd_teacher_topk_workspace_size.argtypes = [i64, i64, i64, i32, i64, ctypes.POINTER(sz)]
+        L.kd_teacher_topk_workspace_size.restype = ctypes.c_int
+        L.kd_teacher_topk.argtypes = [vp, vp, i64, i64, i64, i32, f32, i64, vp, vp, vp, vp, sz, vp,
+                                      vp]
+        L.kd_teacher_topk.restype = ctypes.c_int
         L.kd_entropy_filter_workspace_size.argtypes = [i64, ctypes.POINTER(sz)]
         L.kd_entropy_filter_workspace_size.restype = ctypes.c_int
         L.kd_entropy_filter.argtypes = [vp, vp, i64, i32, f32, i32, i32, vp, vp, vp, sz, vp, vp]
@@ -227,6 +234,25 @@ def kd_topk_kl_backward_residual(h, W, teacher_idx, teacher_logits, teacher_lse,
         T, V, d, K, float(tau), int(chunk), _ptr(lse), _ptr(topk_mass), float(grad_loss), _ptr(dh),
         _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
     _check(rc, "kd_topk_kl_backward_residual")
+
+
+def kd_teacher_topk_workspace_size(T: int, V: int, d: int, K: int, chunk: int) -> int:
+    b = ctypes.c_size_t(0)
+    _check(lib().kd_teacher_topk_workspace_size(T, V, d, K, chunk, ctypes.byref(b)),
+           "kd_teacher_topk_workspace_size")
+    return b.value
+
+
+def kd_teacher_topk(h, W, K, tau, chunk, topk_idx, topk_logits, full_lse=None, *, ws, dev_status,
+                    stream=None):
+    """Per row the K largest logits of h W^T (descending, ties by lower index),
+    their indices, and optionally the full-vocabulary lse of z / tau."""
+    T, d = h.shape
+    V = W.shape[0]
+    rc = lib().kd_teacher_topk(_ptr(h), _ptr(W), T, V, d, int(K), float(tau), int(chunk),
+                               _ptr(topk_idx), _ptr(topk_logits), _ptr(full_lse), _ptr(ws),
+                               ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+    _check(rc, "kd_teacher_topk")
 
 
 def kd_entropy_filter_workspace_size(T: int) -> int:

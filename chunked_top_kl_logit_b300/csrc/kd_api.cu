@@ -13,6 +13,7 @@
 #include "../../include/kd_topk_kl.h"
 #include "kd_filter.cuh"
 #include "kd_kernels.cuh"
+#include "kd_topk_producer.cuh"
 
 using namespace kd;
 
@@ -176,7 +177,8 @@ GemmParams base_params(int a_mn, int b_mn, int BN) {
 }
 
 static_assert(KD_KERNEL_LOGITS_FWD == EPI_FWD && KD_KERNEL_LOGITS_BWD == EPI_DZ &&
-                  KD_KERNEL_DH == EPI_DH && KD_KERNEL_DW == EPI_DW,
+                  KD_KERNEL_DH == EPI_DH && KD_KERNEL_DW == EPI_DW &&
+                  KD_KERNEL_TOPK_PASS1 == EPI_TMAX && KD_KERNEL_TOPK_PASS2 == EPI_TCAND,
               "kernel ids of the timing interface follow the epilogue modes");
 
 // Diagnostic launch timing (kd_timing_*): while recording, each contraction
@@ -294,6 +296,32 @@ void logit_schedule(GemmParams& p, int64_t rows, int64_t V, int64_t d) {
   p.N = static_cast<int>(V);
 }
 
+// Workspace of the teacher top-K producer, for chunks of C rows.
+struct TopkLayout {
+  size_t part, tkeys, theta, theta_val, cnt, cand, total;
+  int64_t C;
+  int n_tiles, cap;
+};
+
+TopkLayout make_topk_layout(int64_t T, int64_t V, int32_t K, int64_t chunk) {
+  TopkLayout L{};
+  L.C = chunk < T ? chunk : T;
+  L.n_tiles = static_cast<int>(cdiv(V, ZBN));
+  // candidates per row: at most (K - 1) full tiles plus the threshold key, or
+  // the whole row when it has fewer than K tiles
+  const int64_t bound = K <= L.n_tiles ? static_cast<int64_t>(K - 1) * ZBN + 1 : V;
+  L.cap = static_cast<int>(bound < V ? bound : V);
+  size_t off = 0;
+  L.part = off;      off += al256(static_cast<size_t>(L.n_tiles) * L.C * 4);
+  L.tkeys = off;     off += al256(static_cast<size_t>(L.C) * L.n_tiles * 8);
+  L.theta = off;     off += al256(static_cast<size_t>(L.C) * 8);
+  L.theta_val = off; off += al256(static_cast<size_t>(L.C) * 4);
+  L.cnt = off;       off += al256(static_cast<size_t>(L.C) * 4);
+  L.cand = off;      off += al256(static_cast<size_t>(L.C) * L.cap * 8);
+  L.total = off;
+  return L;
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------
@@ -345,6 +373,7 @@ const char* kd_topk_kl_status_string(int status) {
     case KD_ERR_INDEX_RANGE: return "teacher index outside [0, V)";
     case KD_ERR_TIMEOUT: return "bounded pipeline wait timed out";
     case KD_ERR_SCRATCH_LIMIT: return "shape needs more than the built-in 32 MiB scratch array";
+    case KD_ERR_INTERNAL: return "internal bound violated (library bug)";
     default: return "unknown status";
   }
 }
@@ -817,6 +846,81 @@ int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* te
     return rc;
   return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, lse, grad_loss, dh, dW,
                           0, dev_status, st);
+}
+
+int kd_teacher_topk_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk,
+                                   size_t* bytes) {
+  const int rc = check_shape(T, V, d, K, chunk);
+  if (rc != KD_OK) return rc;
+  if (!bytes) return KD_ERR_INVALID_ARG;
+  *bytes = make_topk_layout(T, V, K, chunk).total;
+  return KD_OK;
+}
+
+int kd_teacher_topk(const void* h, const void* W, int64_t T, int64_t V, int64_t d, int32_t K,
+                    float tau, int64_t chunk, int32_t* topk_idx, float* topk_logits,
+                    float* full_lse, void* ws, size_t ws_bytes, int32_t* dev_status,
+                    struct CUstream_st* stream) {
+  if (!h || !W || !topk_idx || !topk_logits || !ws || !dev_status) return KD_ERR_INVALID_ARG;
+  if (!(tau > 0.f) || !std::isfinite(tau)) return KD_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws) ||
+      (reinterpret_cast<uintptr_t>(topk_idx) & 3u) ||
+      (reinterpret_cast<uintptr_t>(topk_logits) & 3u) ||
+      (reinterpret_cast<uintptr_t>(full_lse) & 3u) || (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+    return KD_ERR_INVALID_ARG;
+  int rc = check_shape(T, V, d, K, chunk);
+  if (rc != KD_OK) return rc;
+  const TopkLayout L = make_topk_layout(T, V, K, chunk);
+  if (ws_bytes < L.total) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  char* wb = static_cast<char*>(ws);
+  float* part = reinterpret_cast<float*>(wb + L.part);
+  uint64_t* tkeys = reinterpret_cast<uint64_t*>(wb + L.tkeys);
+  uint64_t* theta = reinterpret_cast<uint64_t*>(wb + L.theta);
+  float* theta_val = reinterpret_cast<float*>(wb + L.theta_val);
+  int* cnt = reinterpret_cast<int*>(wb + L.cnt);
+  uint64_t* cand = reinterpret_cast<uint64_t*>(wb + L.cand);
+  if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
+  const float inv_tau = 1.0f / tau;
+  for (int64_t c0 = 0; c0 < T; c0 += L.C) {
+    const int64_t rows = (T - c0) < L.C ? (T - c0) : L.C;
+    const void* hc = static_cast<const __nv_bfloat16*>(h) + c0 * d;
+    CUtensorMap ta, tb;
+    if (!make_map(&ta, hc, d, rows, d, BM) || !make_map(&tb, W, d, V, d, ZBN)) return KD_ERR_CUDA;
+    // pass 1: tile maxima and lse partials
+    GemmParams p = base_params(0, 0, ZBN);
+    logit_schedule(p, rows, V, d);
+    p.status = dev_status;
+    p.inv_tau = inv_tau;
+    p.c_log2 = LOG2E * inv_tau;
+    p.part = part;
+    p.part_ld = rows;
+    p.tkeys = tkeys;
+    if ((rc = launch_gemm<EPI_TMAX>(ta, tb, ta, p, sms, st))) return rc;
+    const unsigned blocks = static_cast<unsigned>(cdiv(rows, TOPK_WARPS));
+    kd_topk_threshold_kernel<<<blocks, 32 * TOPK_WARPS, 0, st>>>(
+        tkeys, part, rows, static_cast<int>(rows), L.n_tiles, K, theta, theta_val,
+        full_lse ? full_lse + c0 : nullptr);
+    if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(rows) * 4, st) != cudaSuccess)
+      return KD_ERR_CUDA;
+    // pass 2: candidates at or above the threshold
+    GemmParams q = base_params(0, 0, ZBN);
+    logit_schedule(q, rows, V, d);
+    q.status = dev_status;
+    q.theta = theta;
+    q.theta_val = theta_val;
+    q.cand = cand;
+    q.cand_cnt = cnt;
+    q.cand_cap = L.cap;
+    if ((rc = launch_gemm<EPI_TCAND>(ta, tb, ta, q, sms, st))) return rc;
+    kd_topk_finalize_kernel<<<blocks, 32 * TOPK_WARPS, 0, st>>>(
+        cand, cnt, L.cap, static_cast<int>(rows), K, topk_idx + c0 * K, topk_logits + c0 * K);
+    if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+  }
+  return KD_OK;
 }
 
 int kd_entropy_filter_workspace_size(int64_t T, size_t* bytes) {

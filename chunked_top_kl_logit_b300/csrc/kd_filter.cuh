@@ -14,14 +14,9 @@
 #include <math_constants.h>
 #include <stdint.h>
 
-namespace kd {
+#include "kd_ptx.cuh"
 
-// Order-preserving map of a finite float to uint32 (-0 is folded into +0 so
-// that equal values get equal keys).
-__device__ __forceinline__ uint32_t float_order_key(float x) {
-  const uint32_t u = __float_as_uint(x + 0.0f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
+namespace kd {
 
 // One warp per row: H_t and its key; rows that are not candidates
 // (valid_in == 0) get key 0, which no finite entropy maps to.

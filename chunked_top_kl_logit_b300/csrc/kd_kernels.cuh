@@ -40,7 +40,16 @@ constexpr float LN2 = 0.6931471805599453f;
 // so the stores run along d and coalesce) and written through the row map /
 // accumulated; they differ only in schedule, and are separate instantiations
 // so that profiles tell them apart.
-enum EpiMode { EPI_FWD = 0, EPI_DZ = 1, EPI_STORE = 2, EPI_DH = 3, EPI_DW = 4 };
+// EPI_TMAX / EPI_TCAND: the two passes of the teacher-side top-K producer.
+enum EpiMode {
+  EPI_FWD = 0,
+  EPI_DZ = 1,
+  EPI_STORE = 2,
+  EPI_DH = 3,
+  EPI_DW = 4,
+  EPI_TMAX = 5,
+  EPI_TCAND = 6
+};
 
 struct GemmParams {
   // schedule: tile t -> (split s, m tile, n tile)
@@ -100,6 +109,16 @@ struct GemmParams {
   // {S, n_tiles*BN} in split_info for the reduction that follows.
   int part_rows, policy_sms;
   int* split_info;
+  // Teacher top-K producer (per row of the launch): pass 1 writes the key of
+  // each vocabulary tile's largest logit to tkeys[row * n_tiles + tile]; pass 2
+  // appends every key >= theta[row] to cand[row * cand_cap + ...], counting in
+  // cand_cnt[row].
+  uint64_t* tkeys;
+  const uint64_t* theta;
+  const float* theta_val;
+  uint64_t* cand;
+  int* cand_cnt;
+  int cand_cap;
 };
 
 // Per-launch schedule, resolved on the device at kernel start.
@@ -618,6 +637,105 @@ __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, co
   mbar_arrive(&tempty[acc]);
 }
 
+// Teacher top-K producer, pass 1 (EPI_TMAX): per (row, vocabulary tile) the
+// key of the tile's largest logit (the lowest index among equal maxima) and
+// the natural-log lse partial of z / tau (for the teacher's full-vocabulary
+// normaliser).
+__device__ __forceinline__ void epi_tmax(const GemmParams& p, const Sched& sc_, const TileCoord& c,
+                                         int acc, uint32_t tmem_row, int r_in_tile,
+                                         uint64_t* tfull, uint64_t* tempty, uint32_t use,
+                                         volatile int* abort_flag, bool& ok) {
+  const int lrow = c.m * BM + r_in_tile;
+  const bool row_ok = lrow < sc_.M;
+  const int v0 = c.n * ZBN;
+  bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
+  ok = __all_sync(0xffffffffu, w);
+  if (!ok) return;
+  tc_fence_after();
+  float m = -CUDART_INF_F;
+  float s = 0.f;
+  float best = -CUDART_INF_F;
+  int bidx = v0;
+#pragma unroll 1
+  for (int cc = 0; cc < ZBN / 32; ++cc) {
+    const int cb = v0 + cc * 32;
+    if (cb >= p.N) break;
+    uint32_t r[32];
+    tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
+    tmem_ld_wait(r);
+    float u[32];
+    float cm = -CUDART_INF_F;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float x = __uint_as_float(r[j]);
+      const bool in = cb + j < p.N;
+      if (in && x > best) {  // ascending j: the first of equal maxima stays
+        best = x;
+        bidx = cb + j;
+      }
+      u[j] = in ? x * p.c_log2 : -CUDART_INF_F;
+      cm = fmaxf(cm, u[j]);
+    }
+    const float mn = fmaxf(m, cm);
+    float cs = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) cs += ex2f(u[j] - mn);
+    s = s * ex2f(m - mn) + cs;
+    m = mn;
+  }
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
+  if (row_ok) {
+    p.part[static_cast<int64_t>(c.n) * p.part_ld + lrow] = (m + lg2f(s)) * LN2;
+    p.tkeys[static_cast<int64_t>(lrow) * sc_.n_tiles + c.n] = logit_key(best, bidx);
+  }
+}
+
+// Teacher top-K producer, pass 2 (EPI_TCAND): every logit whose key is at
+// least the row's threshold becomes a candidate.
+__device__ __forceinline__ void epi_tcand(const GemmParams& p, const Sched& sc_, const TileCoord& c,
+                                          int acc, uint32_t tmem_row, int r_in_tile,
+                                          uint64_t* tfull, uint64_t* tempty, uint32_t use,
+                                          volatile int* abort_flag, bool& ok) {
+  const int lrow = c.m * BM + r_in_tile;
+  const bool row_ok = lrow < sc_.M;
+  const int v0 = c.n * ZBN;
+  uint64_t th = ~0ull;
+  float tv = CUDART_INF_F;
+  if (row_ok) {
+    th = p.theta[lrow];
+    tv = p.theta_val[lrow];
+  }
+  bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
+  ok = __all_sync(0xffffffffu, w);
+  if (!ok) return;
+  tc_fence_after();
+#pragma unroll 1
+  for (int cc = 0; cc < ZBN / 32; ++cc) {
+    const int cb = v0 + cc * 32;
+    if (cb >= p.N) break;
+    uint32_t r[32];
+    tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
+    tmem_ld_wait(r);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float x = __uint_as_float(r[j]);
+      if (x >= tv && cb + j < p.N) {  // rare: only near the row's top-K
+        const uint64_t key = logit_key(x, cb + j);
+        if (key >= th) {
+          const int pos = atomicAdd(p.cand_cnt + lrow, 1);
+          if (pos < p.cand_cap)
+            p.cand[static_cast<int64_t>(lrow) * p.cand_cap + pos] = key;
+          else
+            set_status(p.status, KD_ERR_INTERNAL);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
+}
+
 // ------------------------------------------------------------------ kernel
 
 template <int MODE>
@@ -690,6 +808,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         epi_dz(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else if (MODE == EPI_STORE)
         epi_store(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+      else if (MODE == EPI_TMAX)
+        epi_tmax(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+      else if (MODE == EPI_TCAND)
+        epi_tcand(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else
         epi_store_t(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       if (!ok) break;

@@ -267,6 +267,24 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
+// Order-preserving map of a finite float to uint32 (-0 is folded into +0 so
+// that equal values get equal keys), and its inverse.
+__device__ __forceinline__ uint32_t float_order_key(float x) {
+  const uint32_t u = __float_as_uint(x + 0.0f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float float_from_order_key(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// 64-bit key of a logit at vocabulary index v: larger logit first, then the
+// lower index first; unique per (row, index).
+__device__ __forceinline__ uint64_t logit_key(float z, int v) {
+  return (static_cast<uint64_t>(float_order_key(z)) << 32) |
+         static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(v));
+}
+
 __device__ __forceinline__ float lg2f(float x) {
   float y;
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -67,7 +67,8 @@ typedef enum kd_status {
   KD_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
   KD_ERR_INDEX_RANGE = 5,  /* device: a teacher index is outside [0, V) */
   KD_ERR_TIMEOUT = 6,      /* device: a bounded pipeline wait ran out */
-  KD_ERR_SCRATCH_LIMIT = 7 /* kd_topk_kl_forward_noalloc: shape too big for its scratch */
+  KD_ERR_SCRATCH_LIMIT = 7, /* kd_topk_kl_forward_noalloc: shape too big for its scratch */
+  KD_ERR_INTERNAL = 8       /* device: an internal bound proved false (a library bug) */
 } kd_status;
 
 /*
@@ -195,6 +196,36 @@ int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* te
                                  struct CUstream_st* stream);
 
 /*
+ * Teacher-side top-K cache producer (aipuls.nl summary, section "Summary": the
+ * teacher runs once and its top-100 logits per position are cached offline).
+ * From the teacher's final hidden states h (bf16 [T x d]) and LM-head weight W
+ * (bf16 [V x d]) it writes, per row t, without forming the T x V logits:
+ *
+ *   topk_idx    int32 [T x K]  the K vocabulary indices of the largest
+ *                              z_tv = h_t . W_v, ordered by z descending, equal
+ *                              z by the lower index first (the result is unique)
+ *   topk_logits fp32  [T x K]  those z_tv (raw logits, fp32 accumulation)
+ *   full_lse    fp32  [T]      log sum_v exp(z_tv / tau), or NULL: the
+ *                              teacher_lse that kd_topk_kl_forward_residual takes
+ *
+ * Two passes of the tensor-core logit GEMM per chunk of `chunk` rows: the first
+ * records each 256-column tile's largest logit (and lse partials), a per-row
+ * threshold (the K-th largest tile maximum) bounds the candidates to at most
+ * (K - 1) * 256 + 1 per row, the second collects them, and an exact selection
+ * orders the K largest.  The workspace holds one chunk's candidates:
+ * kd_teacher_topk_workspace_size(...) ~ chunk * 8 * min(V, (K - 1) * 256 + 1)
+ * bytes.  Inputs must be finite.  Limits and errors as kd_topk_kl_forward
+ * (KD_ERR_INTERNAL in *dev_status would mean a candidate bound was exceeded,
+ * which the construction rules out).  Deterministic.
+ */
+int kd_teacher_topk_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk,
+                                   size_t* bytes);
+int kd_teacher_topk(const void* h, const void* W, int64_t T, int64_t V, int64_t d, int32_t K,
+                    float tau, int64_t chunk, int32_t* topk_idx, float* topk_logits,
+                    float* full_lse, void* ws, size_t ws_bytes, int32_t* dev_status,
+                    struct CUstream_st* stream);
+
+/*
  * Teacher-entropy token filter, the producer of the valid mask (asibiont.com
  * rewrite, section "Distillation Token Filtering": score each token by the
  * entropy of the teacher's distribution and keep, per batch, a fixed
@@ -284,11 +315,13 @@ int kd_topk_kl_forward_noalloc(const void* h, const void* W, const int32_t* teac
  *   KD_KERNEL_LOGITS_BWD  backward logit recompute with the gradient epilogue
  *   KD_KERNEL_DH          dh = G W (computed as dh^T = W^T G^T)
  *   KD_KERNEL_DW          dW = G^T h (computed as dW^T = h^T G)
+ *   KD_KERNEL_TOPK_PASS1  teacher top-K producer: logits, tile maxima, lse partials
+ *   KD_KERNEL_TOPK_PASS2  teacher top-K producer: logits, candidate collection
  *
  * kd_timing_start(capacity): creates 2 x capacity CUDA events on the current
  *   device (no device memory is allocated) and starts recording: from then on
  *   every contraction launch that kd_topk_kl_forward / kd_topk_kl_backward
- *   make, from any host thread, is bracketed by an event pair recorded on its
+ *   make (and kd_teacher_topk), from any host thread, is bracketed by an event pair recorded on its
  *   stream, until `capacity` launches have been recorded.  Restarting discards
  *   earlier records.
  * kd_timing_stop(): stops recording; the records stay readable.
@@ -301,7 +334,9 @@ enum {
   KD_KERNEL_LOGITS_FWD = 0,
   KD_KERNEL_LOGITS_BWD = 1,
   KD_KERNEL_DH = 3,
-  KD_KERNEL_DW = 4
+  KD_KERNEL_DW = 4,
+  KD_KERNEL_TOPK_PASS1 = 5,
+  KD_KERNEL_TOPK_PASS2 = 6
 };
 int kd_timing_start(int32_t capacity);
 int kd_timing_stop(void);

@@ -34,7 +34,7 @@ def test_header_symbols_exported():
 
 
 def test_status_strings():
-    for code in range(8):
+    for code in range(9):
         s = kd.status_string(code)
         assert isinstance(s, str) and s and s != "unknown status"
     assert kd.status_string(99) == "unknown status"

@@ -614,3 +614,44 @@ def test_planted_residual_gradient_without_bucket_term(monkeypatch):
     monkeypatch.setattr(RO, "grad_logits_rows", broken)
     with pytest.raises(AssertionError):
         test_residual_gradient_with_autograd(1.0)
+
+
+# --------------------------------------------------------------------------
+# teacher-side top-K cache producer
+# --------------------------------------------------------------------------
+
+from oracle import teacher_topk_oracle as TK  # noqa: E402
+
+
+def test_teacher_topk_bruteforce_python():
+    """Pure-Python selection (no numpy sort) on small random problems with ties."""
+    rng = np.random.default_rng(31)
+    for trial in range(6):
+        T, d, V, K = 5, 4, 40, 7
+        h = rng.integers(-2, 3, size=(T, d)).astype(np.float64)
+        W = rng.integers(-2, 3, size=(V, d)).astype(np.float64)  # many exact ties
+        idx, val, lse = TK.teacher_topk(h, W, K, 1.3)
+        for t in range(T):
+            z = [sum(h[t, j] * W[v, j] for j in range(d)) for v in range(V)]
+            ref = sorted(range(V), key=lambda v: (-z[v], v))[:K]
+            assert list(idx[t]) == ref
+            assert list(val[t]) == [z[v] for v in ref]
+            m = max(z)
+            assert abs(lse[t] - (m / 1.3 + math.log(sum(math.exp((x - m) / 1.3) for x in z)))) < 1e-12
+
+
+def test_teacher_topk_with_torch_topk_and_closed_forms():
+    rng = np.random.default_rng(32)
+    h = rng.standard_normal((9, 16))
+    W = rng.standard_normal((300, 16)) / 4
+    idx, val, lse = TK.teacher_topk(h, W, 25, 2.0)
+    vals, ids = torch.topk(torch.tensor(h @ W.T), 25, dim=1)  # continuous: no ties
+    assert np.array_equal(idx, ids.numpy()) and np.allclose(val, vals.numpy(), atol=0)
+    assert np.allclose(lse, scipy.special.logsumexp(h @ W.T / 2.0, axis=1), atol=1e-12)
+    # W = 0: every logit is 0, the first K indices in order, lse = log V
+    idx0, val0, lse0 = TK.teacher_topk(h, np.zeros_like(W), 10, 0.5)
+    assert np.array_equal(idx0, np.tile(np.arange(10), (9, 1))) and np.all(val0 == 0)
+    assert np.allclose(lse0, math.log(300), atol=1e-12)
+    # K = V: the whole row sorted
+    idx_all, val_all, _ = TK.teacher_topk(h[:2], W[:30], 30, 1.0)
+    assert np.all(np.diff(val_all, axis=1) <= 0) and sorted(idx_all[0]) == list(range(30))
