@@ -32,7 +32,7 @@ __all__ = [
     "KD_ACCUMULATE_DW", "kd_entropy_filter_workspace_size", "kd_entropy_filter",
     "kd_topk_kl_forward_residual", "kd_topk_kl_backward_residual",
     "kd_teacher_topk_workspace_size", "kd_teacher_topk", "PRODUCER_KERNELS",
-    "kd_gemm_bf16_diag", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
+    "kd_gemm_bf16_diag", "kd_gemm_bf16_diag_pair", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
     "KERNELS", "kd_timing_start", "kd_timing_stop", "kd_timing_query", "kd_timing_release",
 ]
 
@@ -102,6 +102,8 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_forward_noalloc.restype = ctypes.c_int
         L.kd_gemm_bf16_diag.argtypes = [vp, vp, vp, i64, i64, i64, i32, i32, vp, vp]
         L.kd_gemm_bf16_diag.restype = ctypes.c_int
+        L.kd_gemm_bf16_diag_pair.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp]
+        L.kd_gemm_bf16_diag_pair.restype = ctypes.c_int
         L.kd_pipeline_wait_selftest.argtypes = [ctypes.c_uint64, vp, vp]
         L.kd_pipeline_wait_selftest.restype = ctypes.c_int
         L.kd_timing_start.argtypes = [i32]
@@ -277,6 +279,13 @@ def kd_gemm_bf16_diag(A, B, C, M, N, Kd, a_mn, b_mn, *, dev_status, stream=None)
     rc = lib().kd_gemm_bf16_diag(_ptr(A), _ptr(B), _ptr(C), M, N, Kd, int(a_mn), int(b_mn),
                                  _ptr(dev_status), _stream(stream))
     _check(rc, "kd_gemm_bf16_diag")
+
+
+def kd_gemm_bf16_diag_pair(A, B, C, M, N, Kd, *, dev_status, stream=None):
+    """C = A B^T on the CTA-pair (cta_group::2) pipeline; A [M, Kd], B [N, Kd] bf16."""
+    rc = lib().kd_gemm_bf16_diag_pair(_ptr(A), _ptr(B), _ptr(C), M, N, Kd, _ptr(dev_status),
+                                      _stream(stream))
+    _check(rc, "kd_gemm_bf16_diag_pair")
 
 
 def kd_pipeline_wait_selftest(limit_ns, *, dev_status, stream=None):

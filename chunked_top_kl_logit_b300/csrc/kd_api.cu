@@ -23,7 +23,7 @@ namespace {
 // than the SM count of whatever device is current, so that results do not
 // depend on the device's SM count.  Grid sizes do use the live SM count.
 constexpr int kPolicySMs = 148;
-constexpr int kRasterGroupRows = 32;  // m tiles per raster group (4096 rows of h in L2)
+constexpr int kRasterGroupRows = 32;  // 128-row tiles per raster group (4096 rows of h in L2)
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -176,9 +176,12 @@ GemmParams base_params(int a_mn, int b_mn, int BN) {
   return p;
 }
 
-static_assert(KD_KERNEL_LOGITS_FWD == EPI_FWD && KD_KERNEL_LOGITS_BWD == EPI_DZ &&
-                  KD_KERNEL_DH == EPI_DH && KD_KERNEL_DW == EPI_DW &&
-                  KD_KERNEL_TOPK_PASS1 == EPI_TMAX && KD_KERNEL_TOPK_PASS2 == EPI_TCAND,
+static_assert(static_cast<int>(KD_KERNEL_LOGITS_FWD) == EPI_FWD &&
+                  static_cast<int>(KD_KERNEL_LOGITS_BWD) == EPI_DZ &&
+                  static_cast<int>(KD_KERNEL_DH) == EPI_DH &&
+                  static_cast<int>(KD_KERNEL_DW) == EPI_DW &&
+                  static_cast<int>(KD_KERNEL_TOPK_PASS1) == EPI_TMAX &&
+                  static_cast<int>(KD_KERNEL_TOPK_PASS2) == EPI_TCAND,
               "kernel ids of the timing interface follow the epilogue modes");
 
 // Diagnostic launch timing (kd_timing_*): while recording, each contraction
@@ -221,24 +224,60 @@ int timing_slot(int kind) {
 }
 
 // `c` is the output tensor map of EPI_DW (ignored by the other modes).
-template <int MODE>
+// PAIR = 1 launches clusters of two CTAs sharing cta_group::2 MMAs; p must
+// then hold a pair schedule (pair_schedule below).
+template <int MODE, int PAIR = 0>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, GemmParams p,
                 int sms, cudaStream_t st) {
   if (p.num_tiles <= 0) return KD_OK;
+  p.pair = PAIR;
   p.epi_smem = MODE == EPI_DW ? 4u * 2u * DW_PIECE_FLOATS * 4u : 0u;
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + p.epi_smem + 256;
-  if (cudaFuncSetAttribute(kd_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(kd_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return KD_ERR_CUDA;
-  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
   const int slot = MODE == EPI_STORE ? -1 : timing_slot(MODE);
-  if (slot >= 0 && cudaEventRecord(timing().recs[slot].start, st) != cudaSuccess)
+  if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
     return KD_ERR_CUDA;
-  kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, c, p);
+  if (PAIR) {
+    const int clusters = p.num_tiles < sms / 2 ? p.num_tiles : sms / 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kd_gemm_kernel<MODE, PAIR>, a, b, c, p) != cudaSuccess)
+      return KD_ERR_CUDA;
+  } else {
+    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
+    kd_gemm_kernel<MODE, PAIR><<<grid, NUM_THREADS, smem, st>>>(a, b, c, p);
+  }
   if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
-  if (slot >= 0 && cudaEventRecord(timing().recs[slot].stop, st) != cudaSuccess)
+  if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
     return KD_ERR_CUDA;
   return KD_OK;
+}
+
+// Turn a one-CTA schedule with K-major operands and 128 x BN tiles into the
+// CTA-pair schedule: 256 x BN tiles per pair, each CTA loading its 128 rows of
+// A and BN/2 rows of B (so B's tensor map box is BN/2 rows), M = 256 MMAs.
+void pair_schedule(GemmParams& p, int group_pairs) {
+  p.a_bytes = BM * BK * 2;
+  p.b_bytes = static_cast<uint32_t>(p.BN / 2) * BK * 2;
+  p.stage_bytes = p.a_bytes + p.b_bytes;
+  p.stages = static_cast<int>((200u * 1024u) / p.stage_bytes);
+  if (p.stages > MAX_STAGES) p.stages = MAX_STAGES;
+  p.idesc = make_idesc_bf16(2 * BM, p.BN, 0, 0);
+  p.m_tiles = static_cast<int>(cdiv(p.M, 2 * BM));
+  p.num_tiles = p.m_tiles * p.n_tiles * p.splits;
+  p.group_m = p.m_tiles < group_pairs ? p.m_tiles : group_pairs;
 }
 
 struct Ws {
@@ -283,7 +322,12 @@ int run_prep(const int32_t* idx, const float* tl, const uint8_t* valid, int64_t 
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
-// Logit-tile schedule shared by the forward and the backward recompute.
+// Logit-tile schedule shared by the forward, the backward recompute and the
+// teacher top-K passes: 128 x 256 tiles, raster groups of 32 row tiles (4096
+// rows of h stay L2-resident), vocabulary-major inside a group.  (The CTA-pair
+// schedule of kd_gemm_bf16_diag_pair computes the same tiles as 256 x 256 pair
+// tiles; under the 1.1 kW power cap it made the whole step 3% slower, so the
+// loss keeps one CTA per tile.)
 void logit_schedule(GemmParams& p, int64_t rows, int64_t V, int64_t d) {
   p.m_tiles = static_cast<int>(cdiv(rows, BM));
   p.n_tiles = static_cast<int>(cdiv(V, ZBN));
@@ -697,6 +741,36 @@ int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t
   p.ld_out = N;
   if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
   return launch_gemm<EPI_STORE>(ta, tb, ta, p, sms, st);
+}
+
+int kd_gemm_bf16_diag_pair(const void* A, const void* B, float* C, int64_t M, int64_t N,
+                           int64_t Kd, int32_t* dev_status, struct CUstream_st* stream) {
+  if (!A || !B || !C || !dev_status) return KD_ERR_INVALID_ARG;
+  if (M < 1 || N < 1 || Kd < 1) return KD_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(B) || !aligned16(C)) return KD_ERR_INVALID_ARG;
+  if (M % 8 || N % 8 || Kd % 8 || M > INT32_MAX || N > INT32_MAX || Kd > INT32_MAX)
+    return KD_ERR_UNSUPPORTED;
+  int sms = 0;
+  int rc = device_sms(&sms);
+  if (rc != KD_OK) return rc;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int BN = N >= 256 ? 256 : static_cast<int>(cdiv(N, 64) * 64);
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, Kd, M, Kd, BM) || !make_map(&tb, B, Kd, N, Kd, BN / 2)) return KD_ERR_CUDA;
+  GemmParams p = base_params(0, 0, BN);
+  p.m_tiles = static_cast<int>(cdiv(M, BM));
+  p.n_tiles = static_cast<int>(cdiv(N, BN));
+  p.k_steps = static_cast<int>(cdiv(Kd, BK));
+  p.ks_per_split = p.k_steps;
+  p.n_fast = 0;
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  pair_schedule(p, 16);
+  p.status = dev_status;
+  p.out = C;
+  p.ld_out = N;
+  if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
+  return launch_gemm<EPI_STORE, 1>(ta, tb, ta, p, sms, st);
 }
 
 int kd_pipeline_wait_selftest(uint64_t limit_ns, int32_t* dev_status,

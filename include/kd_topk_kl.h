@@ -269,6 +269,17 @@ int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t
                       struct CUstream_st* stream);
 
 /*
+ * The same diagnostic product on the CTA-pair pipeline that the logit GEMMs
+ * use: clusters of two CTAs, each 256 x BN tile computed by tcgen05.mma with
+ * cta_group::2 (each CTA holds 128 rows of A and BN/2 rows of B in its shared
+ * memory and 128 rows of the accumulator in its tensor memory).  Both operands
+ * K-major: A bf16 [M x Kd], B bf16 [N x Kd]; C fp32 [M x N].  Limits as
+ * kd_gemm_bf16_diag.
+ */
+int kd_gemm_bf16_diag_pair(const void* A, const void* B, float* C, int64_t M, int64_t N,
+                           int64_t Kd, int32_t* dev_status, struct CUstream_st* stream);
+
+/*
  * Self-test of the failure detection every pipeline wait relies on (the pages
  * describe no failure handling; this checks the library's own bound).  One
  * thread waits on an mbarrier that nothing arrives on, through the same

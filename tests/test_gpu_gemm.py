@@ -36,6 +36,20 @@ def test_gemm_layouts(M, N, Kd, a_mn, b_mn):
     assert err <= 1e-4 * (Kd ** 0.5) * 4, err
 
 
+@pytest.mark.parametrize("M,N,Kd", [(256, 256, 64), (512, 512, 640), (200, 136, 200),
+                                    (1024, 768, 1024), (136, 64, 72), (128, 256, 2880)])
+def test_gemm_cta_pair(M, N, Kd):
+    """The cta_group::2 pipeline (clusters of two CTAs, 256-row tiles)."""
+    Ad, Bd, ref = _operands(M, N, Kd, 0, 0, seed=M * 5 + N + Kd)
+    C = torch.full((M, N), float("nan"), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kd.kd_gemm_bf16_diag_pair(Ad, Bd, C, M, N, Kd, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, kd.status_string(int(st.item()))
+    err = (C.double().cpu() - ref).abs().max().item()
+    assert err <= 1e-4 * (Kd ** 0.5) * 4, err
+
+
 def test_bounded_wait_times_out():
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     kd.kd_pipeline_wait_selftest(20_000_000, dev_status=st)  # 20 ms
