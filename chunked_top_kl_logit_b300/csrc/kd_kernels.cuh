@@ -401,19 +401,31 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
     uint32_t r[32];
     tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
     tmem_ld_wait(r);
-    float u[32];
-    float cm = -CUDART_INF_F;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      u[j] = (cb + j < p.N) ? __uint_as_float(r[j]) * p.c_log2 : -CUDART_INF_F;
-      cm = fmaxf(cm, u[j]);
-    }
-    const float mn = fmaxf(m, cm);
     float cs = 0.f;
+    if (cb + 32 <= p.N) {  // uniform: all 32 columns inside the vocabulary
+      // max on the raw logits (c > 0), then one FFMA + one ex2 per element
+      float cz = __uint_as_float(r[0]);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) cs += ex2f(u[j] - mn);
-    s = s * ex2f(m - mn) + cs;
-    m = mn;
+      for (int j = 1; j < 32; ++j) cz = fmaxf(cz, __uint_as_float(r[j]));
+      const float mn = fmaxf(m, cz * p.c_log2);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) cs += ex2f(fmaf(__uint_as_float(r[j]), p.c_log2, -mn));
+      s = s * ex2f(m - mn) + cs;
+      m = mn;
+    } else {  // the vocabulary ends inside this chunk
+      float u[32];
+      float cm = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        u[j] = (cb + j < p.N) ? __uint_as_float(r[j]) * p.c_log2 : -CUDART_INF_F;
+        cm = fmaxf(cm, u[j]);
+      }
+      const float mn = fmaxf(m, cm);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) cs += ex2f(u[j] - mn);
+      s = s * ex2f(m - mn) + cs;
+      m = mn;
+    }
     const int ce = cb + 32;
     while (__any_sync(0xffffffffu, nxt < ce)) {
       if (nxt < ce) {
@@ -480,7 +492,7 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
     float g[32];
     if (sc != 0.f) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) g[j] = a_row * ex2f(__uint_as_float(r[j]) * p.c_log2 - lb);
+      for (int j = 0; j < 32; ++j) g[j] = a_row * ex2f(fmaf(__uint_as_float(r[j]), p.c_log2, -lb));
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j) g[j] = 0.f;
@@ -494,7 +506,7 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
           uint32_t bits = 0;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) bits = (jj == j) ? r[jj] : bits;
-          add += sc * rq * ex2f(__uint_as_float(bits) * p.c_log2 - lb);
+          add += sc * rq * ex2f(fmaf(__uint_as_float(bits), p.c_log2, -lb));
         }
 #pragma unroll
         for (int jj = 0; jj < 32; ++jj) g[jj] = (jj == j) ? g[jj] + add : g[jj];
