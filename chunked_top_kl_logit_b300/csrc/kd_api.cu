@@ -13,6 +13,7 @@
 #include "../../include/kd_topk_kl.h"
 #include "kd_filter.cuh"
 #include "kd_kernels.cuh"
+#include "kd_pair.cuh"
 #include "kd_topk_producer.cuh"
 
 using namespace kd;
@@ -224,45 +225,49 @@ int timing_slot(int kind) {
 }
 
 // `c` is the output tensor map of EPI_DW (ignored by the other modes).
-// PAIR = 1 launches clusters of two CTAs sharing cta_group::2 MMAs; p must
-// then hold a pair schedule (pair_schedule below).
-template <int MODE, int PAIR = 0>
+template <int MODE>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, GemmParams p,
                 int sms, cudaStream_t st) {
   if (p.num_tiles <= 0) return KD_OK;
-  p.pair = PAIR;
   p.epi_smem = MODE == EPI_DW ? 4u * 2u * DW_PIECE_FLOATS * 4u : 0u;
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + p.epi_smem + 256;
-  if (cudaFuncSetAttribute(kd_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(kd_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return KD_ERR_CUDA;
+  const int grid = p.num_tiles < sms ? p.num_tiles : sms;
   const int slot = MODE == EPI_STORE ? -1 : timing_slot(MODE);
   if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
     return KD_ERR_CUDA;
-  if (PAIR) {
-    const int clusters = p.num_tiles < sms / 2 ? p.num_tiles : sms / 2;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-    cfg.blockDim = dim3(NUM_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, kd_gemm_kernel<MODE, PAIR>, a, b, c, p) != cudaSuccess)
-      return KD_ERR_CUDA;
-  } else {
-    const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-    kd_gemm_kernel<MODE, PAIR><<<grid, NUM_THREADS, smem, st>>>(a, b, c, p);
-  }
+  kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, c, p);
   if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
   if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
     return KD_ERR_CUDA;
   return KD_OK;
+}
+
+// Launch the CTA-pair kernel (clusters of two CTAs) on a pair schedule.
+int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p, int sms,
+                cudaStream_t st) {
+  if (p.num_tiles <= 0) return KD_OK;
+  const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + 256;
+  if (cudaFuncSetAttribute(kd_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return KD_ERR_CUDA;
+  const int clusters = p.num_tiles < sms / 2 ? p.num_tiles : sms / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kd_gemm_pair_kernel, a, b, p) != cudaSuccess) return KD_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
 // Turn a one-CTA schedule with K-major operands and 128 x BN tiles into the
@@ -325,7 +330,7 @@ int run_prep(const int32_t* idx, const float* tl, const uint8_t* valid, int64_t 
 // Logit-tile schedule shared by the forward, the backward recompute and the
 // teacher top-K passes: 128 x 256 tiles, raster groups of 32 row tiles (4096
 // rows of h stay L2-resident), vocabulary-major inside a group.  (The CTA-pair
-// schedule of kd_gemm_bf16_diag_pair computes the same tiles as 256 x 256 pair
+// kernel of kd_gemm_bf16_diag_pair computes the same tiles as 256 x 256 pair
 // tiles; under the 1.1 kW power cap it made the whole step 3% slower, so the
 // loss keeps one CTA per tile.)
 void logit_schedule(GemmParams& p, int64_t rows, int64_t V, int64_t d) {
@@ -770,7 +775,7 @@ int kd_gemm_bf16_diag_pair(const void* A, const void* B, float* C, int64_t M, in
   p.out = C;
   p.ld_out = N;
   if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
-  return launch_gemm<EPI_STORE, 1>(ta, tb, ta, p, sms, st);
+  return launch_pair(ta, tb, p, sms, st);
 }
 
 int kd_pipeline_wait_selftest(uint64_t limit_ns, int32_t* dev_status,

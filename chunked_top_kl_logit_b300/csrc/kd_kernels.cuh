@@ -63,7 +63,6 @@ struct GemmParams {
   int BN;             // tile width (MMA N)
   int stages;
   uint32_t epi_smem;  // shared-memory bytes of the epilogue's staging buffers (EPI_DW)
-  int pair;           // 1: CTA pairs (cta_group::2), 256-row tiles; K-major operands only
   uint32_t a_bytes, b_bytes, stage_bytes;
   uint32_t idesc;
   // epilogue, all modes
@@ -123,11 +122,8 @@ struct GemmParams {
 };
 
 // Per-launch schedule, resolved on the device at kernel start.
-// With CTA pairs, m_tiles counts 256-row pair tiles and a cluster (two
-// consecutive blocks) walks the tiles together.
 struct Sched {
   int m_tiles, n_tiles, num_tiles, k_steps, ks_per_split, splits, M, N;
-  int first, stride;  // tile walk of this CTA (or pair)
 };
 
 // Split count for `tiles` output tiles over `k_steps` contraction steps: the
@@ -152,8 +148,7 @@ __host__ __device__ inline int pick_splits(int tiles, int k_steps, int max_split
 }
 
 __device__ __forceinline__ Sched make_sched(const GemmParams& p) {
-  Sched s{p.m_tiles, p.n_tiles, p.num_tiles, p.k_steps, p.ks_per_split, p.splits, p.M, p.N,
-          static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x)};
+  Sched s{p.m_tiles, p.n_tiles, p.num_tiles, p.k_steps, p.ks_per_split, p.splits, p.M, p.N};
   if (p.dyn_kind != 0) {
     const int rows = max(0, min(*p.dyn_count - p.dyn_base, p.dyn_cap));
     if (p.dyn_kind == 1) {
@@ -179,12 +174,6 @@ __device__ __forceinline__ Sched make_sched(const GemmParams& p) {
       }
       s.num_tiles = s.m_tiles * s.n_tiles * s.splits;
     }
-  }
-  if (p.pair) {
-    s.m_tiles = (s.M + 2 * BM - 1) / (2 * BM);
-    s.num_tiles = s.m_tiles * s.n_tiles * s.splits;
-    s.first = static_cast<int>(blockIdx.x >> 1);
-    s.stride = static_cast<int>(gridDim.x >> 1);
   }
   return s;
 }
@@ -213,28 +202,6 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, const Sche
   return c;
 }
 
-// Tile of this CTA: with CTA pairs the decoded m is a 256-row pair tile and
-// each CTA takes its 128-row half.
-__device__ __forceinline__ TileCoord decode_cta_tile(const GemmParams& p, const Sched& sc, int t,
-                                                     uint32_t rank) {
-  TileCoord c = decode_tile(p, sc, t);
-  if (p.pair) c.m = 2 * c.m + static_cast<int>(rank);
-  return c;
-}
-
-// Hand an accumulator back to the MMA issuer once this thread's TMEM reads are
-// done: every epilogue thread arrives (128 per CTA), or with CTA pairs one
-// lane per warp arrives on the leader CTA's barrier (8 per pair).
-__device__ __forceinline__ void release_acc(const GemmParams& p, uint64_t* bar) {
-  tc_fence_before();
-  if (p.pair) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive_cluster(mapa_shared(smem_u32(bar), 0));
-  } else {
-    mbar_arrive(bar);
-  }
-}
-
 // First position in the ascending row `s[0..K)` whose value is >= key.
 __device__ __forceinline__ int lower_bound_row(const int* __restrict__ s, int K, int key) {
   int lo = 0, hi = K;
@@ -247,72 +214,50 @@ __device__ __forceinline__ int lower_bound_row(const int* __restrict__ s, int K,
 
 // ------------------------------------------------------------------ roles
 
-template <int PAIR>
 __device__ __forceinline__ void producer_role(const GemmParams& p, const Sched& sc,
                                               const CUtensorMap* tmA,
                                               const CUtensorMap* tmB, uint8_t* smem,
                                               uint64_t* full, uint64_t* empty,
-                                              volatile int* abort_flag, uint32_t rank) {
+                                              volatile int* abort_flag) {
   tma_prefetch_desc(tmA);
   tma_prefetch_desc(tmB);
   int stage = 0;
   uint32_t phase = 0;
   int issued = 0;
   bool ok = true;
-  for (int t = sc.first; t < sc.num_tiles && ok; t += sc.stride) {
-    const TileCoord c = decode_cta_tile(p, sc, t, rank);
+  for (int t = blockIdx.x; t < sc.num_tiles && ok; t += gridDim.x) {
+    const TileCoord c = decode_tile(p, sc, t);
     const int kb = c.s * sc.ks_per_split;
     const int ke = min(sc.k_steps, kb + sc.ks_per_split);
     for (int ks = kb; ks < ke; ++ks) {
       if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
       uint8_t* sa = smem + static_cast<size_t>(stage) * p.stage_bytes;
       uint8_t* sb = sa + p.a_bytes;
+      mbar_arrive_expect_tx(&full[stage], p.stage_bytes);
       const int k0 = ks * BK;
-      if (PAIR) {
-        // both CTAs' bytes complete on the leader's barrier, which the leader arms
-        if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2u * p.stage_bytes);
-        const uint32_t fbar = mapa_shared(smem_u32(&full[stage]), 0);
-        tma_load_2d_pair(sa, tmA, fbar, k0, c.m * BM);
-        tma_load_2d_pair(sb, tmB, fbar, k0, c.n * p.BN + static_cast<int>(rank) * (p.BN / 2));
+      if (!p.a_mn) {
+        tma_load_2d(sa, tmA, &full[stage], k0, c.m * BM);
       } else {
-        mbar_arrive_expect_tx(&full[stage], p.stage_bytes);
-        if (!p.a_mn) {
-          tma_load_2d(sa, tmA, &full[stage], k0, c.m * BM);
-        } else {
-          tma_load_2d(sa, tmA, &full[stage], c.m * BM, k0);
-          tma_load_2d(sa + 8192, tmA, &full[stage], c.m * BM + 64, k0);
-        }
-        if (!p.b_mn) {
-          tma_load_2d(sb, tmB, &full[stage], k0, c.n * p.BN);
-        } else {
-          for (int j = 0; j < p.BN / 64; ++j)
-            tma_load_2d(sb + j * 8192, tmB, &full[stage], c.n * p.BN + 64 * j, k0);
-        }
+        tma_load_2d(sa, tmA, &full[stage], c.m * BM, k0);
+        tma_load_2d(sa + 8192, tmA, &full[stage], c.m * BM + 64, k0);
+      }
+      if (!p.b_mn) {
+        tma_load_2d(sb, tmB, &full[stage], k0, c.n * p.BN);
+      } else {
+        for (int j = 0; j < p.BN / 64; ++j)
+          tma_load_2d(sb + j * 8192, tmB, &full[stage], c.n * p.BN + 64 * j, k0);
       }
       ++issued;
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
   }
   if (!ok) {
-    if (!PAIR || rank == 0) {
-      // let the loads this thread armed land before the CTA leaves (with pairs
-      // the leader's barrier also counts the other CTA's bytes)
-      for (int i = max(0, issued - p.stages); i < issued; ++i)
-        mbar_wait_drain(&full[i % p.stages], static_cast<uint32_t>((i / p.stages) & 1));
-    } else {
-      __nanosleep(200000);  // the other CTA's barrier counts these loads
-    }
-  } else if (PAIR) {
-    // every stage's last fill has been released by the leader's MMA commits
-    // (arrivals into this CTA's barriers) before the pair tears down
-    for (int i = 0; i < p.stages; ++i) {
-      if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.status)) break;
-      if (++stage == p.stages) { stage = 0; phase ^= 1u; }
-    }
+    // let the loads this thread started land before the CTA leaves
+    for (int i = max(0, issued - p.stages); i < issued; ++i)
+      mbar_wait_drain(&full[i % p.stages], static_cast<uint32_t>((i / p.stages) & 1));
   }
 }
 
-template <int PAIR>
 __device__ __forceinline__ void mma_role(const GemmParams& p, const Sched& sc, uint8_t* smem,
                                          uint64_t* full,
                                          uint64_t* empty, uint64_t* tfull, uint64_t* tempty,
@@ -327,7 +272,7 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, const Sched& sc, u
   uint32_t phase = 0;
   bool ok = true;
   int lt = 0;
-  for (int t = sc.first; t < sc.num_tiles; t += sc.stride, ++lt) {
+  for (int t = blockIdx.x; t < sc.num_tiles; t += gridDim.x, ++lt) {
     const TileCoord c = decode_tile(p, sc, t);
     const int kb = c.s * sc.ks_per_split;
     const int ke = min(sc.k_steps, kb + sc.ks_per_split);
@@ -349,21 +294,16 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, const Sched& sc, u
       for (int kk = 0; kk < BK / 16; ++kk) {
         const uint64_t ad = make_sdesc(sa + kk * a_adv, a_lbo, 1024u);
         const uint64_t bd = make_sdesc(sb + kk * b_adv, b_lbo, 1024u);
-        if (PAIR)
-          umma_bf16_pair(d_tmem, ad, bd, p.idesc, (ks > kb || kk > 0) ? 1u : 0u);
-        else
-          umma_bf16(d_tmem, ad, bd, p.idesc, (ks > kb || kk > 0) ? 1u : 0u);
+        umma_bf16(d_tmem, ad, bd, p.idesc, (ks > kb || kk > 0) ? 1u : 0u);
       }
-      // frees the stage (in both CTAs of a pair) once these MMAs have read it
-      if (PAIR) umma_commit_pair_both(&empty[stage]); else umma_commit(&empty[stage]);
+      umma_commit(&empty[stage]);  // frees the stage once these MMAs have read it
       if (++stage == p.stages) { stage = 0; phase ^= 1u; }
     }
     if (!ok) break;
-    // accumulator ready for the epilogue (of both CTAs of a pair)
-    if (PAIR) umma_commit_pair_both(&tfull[acc]); else umma_commit(&tfull[acc]);
+    umma_commit(&tfull[acc]);      // accumulator ready for the epilogue
   }
   if (!ok) {
-    if (PAIR) umma_commit_pair_both(drain); else umma_commit(drain);
+    umma_commit(drain);
     mbar_wait_drain(drain, 0);
   }
 }
@@ -440,7 +380,8 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
       }
     }
   }
-  release_acc(p, &tempty[acc]);
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
   if (row_ok) p.part[static_cast<int64_t>(c.n) * p.part_ld + grow] = (m + lg2f(s)) * LN2;
 }
 
@@ -532,7 +473,8 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
       }
     }
   }
-  release_acc(p, &tempty[acc]);
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
 }
 
 // fp32 tile store, optionally accumulating into the existing output.
@@ -585,7 +527,8 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const Sched& sc_,
       }
     }
   }
-  release_acc(p, &tempty[acc]);
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
 }
 
 // Transposed fp32 tile store for the gradient contractions.  The tile's rows
@@ -645,7 +588,8 @@ __device__ __forceinline__ void epi_store_t(const GemmParams& p, const Sched& sc
         if (j < ncols) base[static_cast<int64_t>(orow[j]) * p.ld_out + m] = __uint_as_float(r[j]) + o[j];
     }
   }
-  release_acc(p, &tempty[acc]);
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
 }
 
 // dW epilogue (EPI_DW): dW^T tile = h^T G, rows = hidden units, columns =
@@ -701,7 +645,8 @@ __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, co
     }
     ++piece;
   }
-  release_acc(p, &tempty[acc]);
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
 }
 
 // Teacher top-K producer, pass 1 (EPI_TMAX): per (row, vocabulary tile) the
@@ -750,7 +695,8 @@ __device__ __forceinline__ void epi_tmax(const GemmParams& p, const Sched& sc_, 
     s = s * ex2f(m - mn) + cs;
     m = mn;
   }
-  release_acc(p, &tempty[acc]);
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
   if (row_ok) {
     p.part[static_cast<int64_t>(c.n) * p.part_ld + lrow] = (m + lg2f(s)) * LN2;
     p.tkeys[static_cast<int64_t>(lrow) * sc_.n_tiles + c.n] = logit_key(best, bidx);
@@ -798,13 +744,13 @@ __device__ __forceinline__ void epi_tcand(const GemmParams& p, const Sched& sc_,
       }
     }
   }
-  release_acc(p, &tempty[acc]);
+  tc_fence_before();
+  mbar_arrive(&tempty[acc]);
 }
 
 // ------------------------------------------------------------------ kernel
 
-// PAIR = 1: launched in clusters of two CTAs (cta_group::2 MMAs, p.pair = 1).
-template <int MODE, int PAIR>
+template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
@@ -825,7 +771,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -833,21 +778,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], PAIR ? 8 : 128);  // pairs: one lane per epilogue warp, two CTAs
+      mbar_init(&tempty[a], 128);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (PAIR) cluster_sync();  // both CTAs' barriers exist before either touches the other's
   if (warp == 1) {
-    if (PAIR) {
-      tmem_alloc_pair(tmem_slot, TMEM_COLS);
-      tmem_relinquish_pair();
-    } else {
-      tmem_alloc(tmem_slot, TMEM_COLS);
-      tmem_relinquish();
-    }
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
@@ -856,10 +795,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   const Sched sc = make_sched(p);
   if (warp == 0) {
-    if (lane == 0) producer_role<PAIR>(p, sc, &tmA, &tmB, smem, full, empty, abort_flag, rank);
+    if (lane == 0) producer_role(p, sc, &tmA, &tmB, smem, full, empty, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0)
-      mma_role<PAIR>(p, sc, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
+    if (lane == 0) mma_role(p, sc, smem, full, empty, tfull, tempty, drain, tmem_base, abort_flag);
   } else {
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int r_in_tile = q * 32 + lane;
@@ -869,8 +807,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t piece = 0;
     float* my_stage = epi_stage + q * 2 * DW_PIECE_FLOATS;
     if (MODE == EPI_DW && lane == 0) tma_prefetch_desc(&tmC);
-    for (int t = sc.first; t < sc.num_tiles; t += sc.stride, ++lt) {
-      const TileCoord c = decode_cta_tile(p, sc, t, rank);
+    for (int t = blockIdx.x; t < sc.num_tiles; t += gridDim.x, ++lt) {
+      const TileCoord c = decode_tile(p, sc, t);
       const int acc = lt & 1;
       const uint32_t use = static_cast<uint32_t>(lt >> 1);
       if (MODE == EPI_DW)
@@ -895,13 +833,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (PAIR) cluster_sync();  // no cross-CTA access is left in flight
   if (warp == 1) {
     tc_fence_after();
-    if (PAIR)
-      tmem_dealloc_pair(tmem_base, TMEM_COLS);
-    else
-      tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
