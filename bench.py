@@ -577,7 +577,7 @@ def main(argv=None):
                     help="split: kd_topk_kl_forward + kd_topk_kl_backward per step; "
                          "fused: one kd_topk_kl_forward_backward call per step")
     ap.add_argument("--cpu-rows", type=int, default=1024)
-    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--ref-rows", type=int, default=256)
     args = ap.parse_args(argv)
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
