@@ -1,17 +1,21 @@
 // Device kernels of the fused top-K KL loss.
 //
 // The contraction kernel is one persistent, warp-specialised tcgen05 GEMM
-// (tile 128 x BN x 64, bf16 in, fp32 accumulate in TMEM) shared by the four
-// contractions of the method:
+// (tile 128 x BN x 64, bf16 in, fp32 accumulate in TMEM) shared by the
+// contractions of the method and of the teacher-side cache producer:
 //
-//   forward   z = h W^T tile by tile      -> epilogue EPI_FWD: online log-sum-exp
-//                                            partial per (row, vocab tile) and
-//                                            the gather of z at the row's cached
-//                                            teacher indices
-//   backward  z = h_c W^T again (chunk c) -> epilogue EPI_DZ: G = s (q - scatter p)/tau
-//                                            written as bf16 into the chunk buffer
-//             dh_c = G_c W                -> epilogue EPI_STORE (split over V)
-//             dW  += G_c^T h_c            -> epilogue EPI_STORE (accumulate)
+//   forward   z = h W^T tile by tile       -> EPI_FWD: online log-sum-exp partial
+//                                             per (row, vocab tile) and the gather
+//                                             of z at the row's cached indices
+//   backward  z = h_c W^T again (chunk c)  -> EPI_DZ: G = s (q - scatter p) / tau
+//                                             as bf16 into the chunk buffer
+//             dh_c^T = W^T G_c^T           -> EPI_DH: transposed store through the
+//                                             valid-row map (split over V on demand)
+//             dW^T  += h_c^T G_c           -> EPI_DW: TMA store / reduce-add of
+//                                             staged 32 x 32 pieces
+//   teacher   z = h_t W_t^T, two passes    -> EPI_TMAX (tile maxima, lse partials)
+//                                             and EPI_TCAND (candidates)
+//   (diagnostic C = A B^T                  -> EPI_STORE)
 //
 // Warp roles (192 threads): warp 0 issues TMA loads into a ring of shared
 // memory stages, warp 1 owns TMEM and issues tcgen05.mma from one thread,
