@@ -199,3 +199,28 @@ def test_grad_loss_scales():
     b = run_gpu(x, 100, grad_loss=-0.25)
     assert rel_l2(b["dh"], -0.25 * a["dh"]) <= 1e-2
     assert rel_l2(b["dW"], -0.25 * a["dW"]) <= 1e-2
+
+
+def test_large_k():
+    """K = 2048 cached entries per row (a quarter of the vocabulary): the rank
+    sort of the teacher entries and the gather / scatter walk over many entries
+    per vocabulary tile."""
+    x = make_inputs(workload("small_4k", T=96, d=128, V=8192, K=2048, tau=1.0,
+                             idx_kind="uniform"))
+    gpu = run_gpu(x, 64)
+    ref = oracle_all(x)
+    assert_forward_parity(gpu, ref)
+    assert rel_l2(gpu["dh"], ref["dh"]) <= GRAD_RL2
+    assert rel_l2(gpu["dW"], ref["dW"]) <= GRAD_RL2
+
+
+def test_wide_hidden_and_ragged_vocab():
+    """d = 4096 (64 contraction steps) with V = 3000 (a ragged last vocabulary
+    tile) and a chunk that is not a multiple of the tile height."""
+    x = make_inputs(workload("small_4k", T=333, d=4096, V=3000, K=24, tau=0.75,
+                             idx_kind="uniform"))
+    gpu = run_gpu(x, 150)
+    ref = oracle_all(x)
+    assert_forward_parity(gpu, ref)
+    assert rel_l2(gpu["dh"], ref["dh"]) <= GRAD_RL2
+    assert rel_l2(gpu["dW"], ref["dW"]) <= GRAD_RL2

@@ -145,3 +145,13 @@ def test_producer_feeds_residual_loss_teacher_equals_student():
     # the forward's own lse equals the producer's normaliser
     assert (lse - tlse).abs().max().item() <= 1e-5
     assert dh.abs().max().item() <= 1e-5 and dW.abs().max().item() <= 1e-5
+
+
+def test_producer_k_larger_than_tile_count():
+    """K = 1000 with 32 vocabulary tiles: every logit is a candidate and the
+    selection orders 1000 of 8192 per row."""
+    g = torch.Generator().manual_seed(17)
+    T, V, d, K = 64, 8192, 128, 1000
+    h = torch.randn(T, d, generator=g).to(torch.bfloat16)
+    W = (torch.randn(V, d, generator=g) / math.sqrt(d)).to(torch.bfloat16)
+    check_against_oracle(h, W, K, 1.0, 64)
