@@ -25,6 +25,7 @@ namespace {
 // depend on the device's SM count.  Grid sizes do use the live SM count.
 constexpr int kPolicySMs = 148;
 constexpr int kRasterGroupRows = 32;  // 128-row tiles per raster group (4096 rows of h in L2)
+constexpr uint32_t kMaxDynSmem = 232448;  // opt-in dynamic shared memory per block (sm_100 family)
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -64,7 +65,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, 
 // box = box_inner x box_outer, no swizzle: the dW output of the TMA
 // store / reduce-add epilogue.
 bool make_map_f32(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, uint64_t ld,
-                  uint32_t box_inner, uint32_t box_outer) {
+                  uint32_t box_inner, uint32_t box_outer, bool swizzle128 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {inner, outer};
@@ -72,7 +73,8 @@ bool make_map_f32(CUtensorMap* m, void* base, uint64_t inner, uint64_t outer, ui
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -97,6 +99,14 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 constexpr int kMaxDhSplits = 4;
 constexpr int kGradBN = 256;  // gradient contractions: 128 hidden units x 256 rows per tile
 
+// Tile width of the dW contraction over the hidden units: the widest multiple
+// of 16 up to 256 that divides d (d = 2880 -> 240), so no column is padding.
+int dw_tile_width(int64_t d) {
+  for (int bn = 256; bn >= 16; bn -= 16)
+    if (d % bn == 0) return bn;
+  return 64;
+}
+
 int dh_max_splits(int64_t V) {
   const int64_t ks = cdiv(V, BK);
   int s = 1;
@@ -107,11 +117,12 @@ int dh_max_splits(int64_t V) {
 struct Layout {
   size_t nvalid, losspart, sidx, sp, sslot, tterm, resid;  // shared by both passes
   size_t zg, part;                                  // forward
-  size_t rowmap, split_info, hc, dz, dhpart;        // backward
+  size_t rowmap, split_info, hc, hct, dz, dhpart;   // backward
   size_t fwd_total, bwd_total;
   int64_t rows_chunk;
   int dh_splits;      // largest split count of the dh contraction
   int64_t part_rows;  // rows of dh partials the split blocks may use
+  int64_t hct_ld;     // row pitch (elements) of the transposed h chunk
 };
 
 Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
@@ -135,6 +146,8 @@ Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
   L.rowmap = off;     off += al256(static_cast<size_t>(T) * 4);
   L.split_info = off; off += 256;
   L.hc = off;         off += al256(static_cast<size_t>(L.rows_chunk * d) * 2);
+  L.hct_ld = cdiv(L.rows_chunk, 8) * 8;  // 16-byte row pitch for the TMA
+  L.hct = off;        off += al256(static_cast<size_t>(L.hct_ld * d) * 2);
   L.dz = off;         off += al256(static_cast<size_t>(L.rows_chunk * V) * 2);
   L.dhpart = off;     off += al256(static_cast<size_t>(L.part_rows * d) * 4);
   L.bwd_total = off;
@@ -224,12 +237,16 @@ int timing_slot(int kind) {
   return t.used++;
 }
 
-// `c` is the output tensor map of EPI_DW (ignored by the other modes).
+// `c` / `dm` are the output tensor maps of EPI_DW (32- and 16-column pieces;
+// ignored by the other modes).
 template <int MODE>
-int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, GemmParams p,
-                int sms, cudaStream_t st) {
+int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                const CUtensorMap& dm, GemmParams p, int sms, cudaStream_t st) {
   if (p.num_tiles <= 0) return KD_OK;
   p.epi_smem = MODE == EPI_DW ? 4u * 2u * DW_PIECE_FLOATS * 4u : 0u;
+  // the stage ring shares the opt-in shared-memory limit with the staging
+  const int fit = static_cast<int>((kMaxDynSmem - 1024u - 256u - p.epi_smem) / p.stage_bytes);
+  if (p.stages > fit) p.stages = fit;
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + p.epi_smem + 256;
   if (cudaFuncSetAttribute(kd_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
@@ -238,7 +255,7 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c
   const int slot = MODE == EPI_STORE ? -1 : timing_slot(MODE);
   if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
     return KD_ERR_CUDA;
-  kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, c, p);
+  kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, c, dm, p);
   if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
   if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
     return KD_ERR_CUDA;
@@ -444,10 +461,10 @@ int kd_topk_kl_launch_count(int64_t T, int64_t V, int64_t d, int32_t K, int64_t 
   const Layout L = make_layout(T, V, d, K, chunk);
   const int64_t chunks = cdiv(T, L.rows_chunk);
   if (fwd_launches) *fwd_launches = 4;  // prep, logit GEMM, combine, loss
-  // prep + row compaction, then per chunk: row gather, recompute, dh, [dh split
-  // reduce], dW
+  // prep + row compaction, then per chunk: row gather (plain and transposed),
+  // recompute, dh, [dh split reduce], dW
   if (bwd_launches)
-    *bwd_launches = static_cast<int32_t>(2 + chunks * (L.dh_splits > 1 ? 5 : 4));
+    *bwd_launches = static_cast<int32_t>(2 + chunks * (L.dh_splits > 1 ? 6 : 5));
   return KD_OK;
 }
 
@@ -482,7 +499,7 @@ int enqueue_forward(const void* h, const void* W, const uint8_t* valid, int64_t 
   p.part = part;
   p.zg = zg;
   p.gidx = gathered_idx;
-  if ((rc = launch_gemm<EPI_FWD>(ta, tb, ta, p, sms, st))) return rc;
+  if ((rc = launch_gemm<EPI_FWD>(ta, tb, ta, ta, p, sms, st))) return rc;
 
   const int nb = static_cast<int>(cdiv(T, 256));
   kd_combine_kernel<<<nb, 256, 0, st>>>(part, p.n_tiles, static_cast<int>(T), K, w.sp, zg,
@@ -504,6 +521,7 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
   char* wb = static_cast<char*>(ws);
   int* rowmap = reinterpret_cast<int*>(wb + L.rowmap);
   __nv_bfloat16* hc = reinterpret_cast<__nv_bfloat16*>(wb + L.hc);
+  __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(wb + L.hct);
   __nv_bfloat16* dz = reinterpret_cast<__nv_bfloat16*>(wb + L.dz);
   float* dhpart = reinterpret_cast<float*>(wb + L.dhpart);
   int* split_info = reinterpret_cast<int*>(wb + L.split_info);
@@ -523,10 +541,16 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
     CUtensorMap ta, tb;
     const int gblocks = sms * 4;
 
-    // (0) the chunk's valid rows of h, zero-padded to C rows
+    // (0) the chunk's valid rows of h, zero-padded to C rows, and transposed
     kd_gather_rows_kernel<<<gblocks, 256, 0, st>>>(
         static_cast<const uint4*>(h), rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
         static_cast<int>(d / 8), reinterpret_cast<uint4*>(hc));
+    kd_gather_rows_t_kernel<<<dim3(static_cast<unsigned>(cdiv(d, 32)),
+                                   static_cast<unsigned>(cdiv(C, 32))),
+                              dim3(32, 8), 0, st>>>(static_cast<const __nv_bfloat16*>(h), rowmap,
+                                                    w.nvalid, static_cast<int>(c0),
+                                                    static_cast<int>(C), static_cast<int>(L.hct_ld),
+                                                    static_cast<int>(d), hct);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
 
     // (1) recompute the chunk's logit tiles and write G as bf16
@@ -554,7 +578,7 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
     p.dyn_kind = 1;
     p.rowmap = rowmap;
     p.rowmap_base = static_cast<int>(c0);
-    if ((rc = launch_gemm<EPI_DZ>(ta, tb, ta, p, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_DZ>(ta, tb, ta, ta, p, sms, st))) return rc;
 
     // (2) dh rows of the chunk, computed transposed: dh_c^T = W^T G_c^T, so a
     // tile is 128 hidden units x 256 chunk rows (A = W as an MN-major operand,
@@ -586,7 +610,7 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
     q.part_rows = static_cast<int>(L.part_rows);
     q.policy_sms = kPolicySMs;
     q.split_info = split_info;
-    if ((rc = launch_gemm<EPI_DH>(ta, tb, ta, q, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_DH>(ta, tb, ta, ta, q, sms, st))) return rc;
     if (S > 1) {
       kd_split_reduce_rows_kernel<<<gblocks, 256, 0, st>>>(
           dh, dhpart, split_info, rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
@@ -594,23 +618,25 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
       if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
     }
 
-    // (3) dW (+)= G_c^T h_c, computed transposed: dW^T = h_c^T G_c with tiles of
-    // 128 hidden units x 256 vocabulary rows (both operands MN-major), the
-    // contraction running over the chunk's valid rows.
-    CUtensorMap tc;
-    if (!make_map(&ta, hc, d, C, d, 64) || !make_map(&tb, dz, V, C, V, 64) ||
-        !make_map_f32(&tc, dW, d, V, d, 32, 32))
+    // (3) dW (+)= G_c^T h_c: tiles of 128 vocabulary rows x BNw hidden units
+    // (A = G as an MN-major operand, B = h_c^T K-major), the contraction over
+    // the chunk's valid rows; 32 x 32 pieces of the tile are stored or
+    // reduce-added into dW by the TMA.
+    const int BNw = dw_tile_width(d);
+    CUtensorMap tc, td;
+    if (!make_map(&ta, dz, V, C, V, 64) || !make_map(&tb, hct, C, d, L.hct_ld, static_cast<uint32_t>(BNw)) ||
+        !make_map_f32(&tc, dW, d, V, d, 32, 32, true) || !make_map_f32(&td, dW, d, V, d, 16, 32))
       return KD_ERR_CUDA;
-    GemmParams r = base_params(1, 1, kGradBN);
-    r.m_tiles = static_cast<int>(cdiv(d, BM));
-    r.n_tiles = static_cast<int>(cdiv(V, kGradBN));
+    GemmParams r = base_params(1, 0, BNw);
+    r.m_tiles = static_cast<int>(cdiv(V, BM));
+    r.n_tiles = static_cast<int>(d / BNw);
     r.num_tiles = r.m_tiles * r.n_tiles;
     r.k_steps = static_cast<int>(cdiv(C, BK));
     r.ks_per_split = r.k_steps;
-    r.n_fast = 0;
-    r.group_m = r.m_tiles;                    // hidden-unit tiles fastest: G slabs shared
-    r.M = static_cast<int>(d);
-    r.N = static_cast<int>(V);
+    r.n_fast = 1;                             // hidden-unit tiles fastest: G slabs shared
+    r.group_m = 1;
+    r.M = static_cast<int>(V);
+    r.N = static_cast<int>(d);
     r.status = dev_status;
     r.out = dW;
     r.out2 = nullptr;
@@ -620,7 +646,7 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
     r.dyn_base = static_cast<int>(c0);
     r.dyn_cap = static_cast<int>(C);
     r.dyn_kind = 2;
-    if ((rc = launch_gemm<EPI_DW>(ta, tb, tc, r, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_DW>(ta, tb, tc, td, r, sms, st))) return rc;
   }
   return KD_OK;
 }
@@ -745,7 +771,7 @@ int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t
   p.out = C;
   p.ld_out = N;
   if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
-  return launch_gemm<EPI_STORE>(ta, tb, ta, p, sms, st);
+  return launch_gemm<EPI_STORE>(ta, tb, ta, ta, p, sms, st);
 }
 
 int kd_gemm_bf16_diag_pair(const void* A, const void* B, float* C, int64_t M, int64_t N,
@@ -978,7 +1004,7 @@ int kd_teacher_topk(const void* h, const void* W, int64_t T, int64_t V, int64_t 
     p.part = part;
     p.part_ld = rows;
     p.tkeys = tkeys;
-    if ((rc = launch_gemm<EPI_TMAX>(ta, tb, ta, p, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_TMAX>(ta, tb, ta, ta, p, sms, st))) return rc;
     const unsigned blocks = static_cast<unsigned>(cdiv(rows, TOPK_WARPS));
     kd_topk_threshold_kernel<<<blocks, 32 * TOPK_WARPS, 0, st>>>(
         tkeys, part, rows, static_cast<int>(rows), L.n_tiles, K, theta, theta_val,
@@ -994,7 +1020,7 @@ int kd_teacher_topk(const void* h, const void* W, int64_t T, int64_t V, int64_t 
     q.cand = cand;
     q.cand_cnt = cnt;
     q.cand_cap = L.cap;
-    if ((rc = launch_gemm<EPI_TCAND>(ta, tb, ta, q, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_TCAND>(ta, tb, ta, ta, q, sms, st))) return rc;
     kd_topk_finalize_kernel<<<blocks, 32 * TOPK_WARPS, 0, st>>>(
         cand, cnt, L.cap, static_cast<int>(rows), K, topk_idx + c0 * K, topk_logits + c0 * K);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;

@@ -596,11 +596,15 @@ __device__ __forceinline__ void epi_store_t(const GemmParams& p, const Sched& sc
   mbar_arrive(&tempty[acc]);
 }
 
-// dW epilogue (EPI_DW): dW^T tile = h^T G, rows = hidden units, columns =
-// vocabulary rows.  Each epilogue warp owns 32 hidden units and moves its part
-// of the tile 32 vocabulary rows at a time through its own two 4 KB staging
-// buffers; one lane then hands the piece to the TMA: a tensor store for the
-// first chunk, a tensor reduce-add (the L2 adds it to dW) for later chunks.
+// dW epilogue (EPI_DW): dW tile = G_c^T h_c, rows = vocabulary rows (TMEM
+// lanes), columns = hidden units.  Each epilogue warp owns 32 vocabulary rows
+// and moves its part of the tile 32 hidden units at a time through its own two
+// 4 KB staging buffers, laid out as the TMA's 128-byte swizzle expects (the
+// 16-byte chunk j of row r sits at chunk j ^ (r % 8), so the row-per-lane
+// stores do not collide in shared-memory banks); one lane then hands the piece
+// to the TMA: a tensor store for the first chunk, a tensor reduce-add (the L2
+// adds it to dW) for later chunks.  A tile width that is an odd multiple of 16
+// ends with a 16-column piece, staged unswizzled for its own tensor map (tmD).
 // Each output element has exactly one owner per launch, so the sum is
 // deterministic.  No barrier spans warps, so a warp that leaves early on an
 // abort cannot leave another waiting.
@@ -609,11 +613,11 @@ constexpr int DW_PIECE_FLOATS = 32 * 32;
 __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, const TileCoord& c,
                                        int acc, uint32_t tmem_row, int q, uint64_t* tfull,
                                        uint64_t* tempty, uint32_t use, volatile int* abort_flag,
-                                       bool& ok, const CUtensorMap* tmC, float* stage_buf,
-                                       uint32_t& piece) {
+                                       bool& ok, const CUtensorMap* tmC, const CUtensorMap* tmD,
+                                       float* stage_buf, uint32_t& piece) {
   const int lane = threadIdx.x & 31;
-  const int mw = c.m * BM + q * 32;       // first hidden unit of this warp
-  const bool warp_ok = mw < sc_.M;        // d % 64 == 0: the warp is all in or all out
+  const int vw = c.m * BM + q * 32;       // first vocabulary row of this warp
+  const bool warp_ok = vw < sc_.M;        // rows past V are clipped by the TMA
   const int n0 = c.n * p.BN;
   const bool accum = p.accumulate != 0;
   const bool kempty = sc_.k_steps == 0;   // no valid row in this chunk
@@ -621,10 +625,12 @@ __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, co
   ok = __all_sync(0xffffffffu, w);
   if (!ok) return;
   tc_fence_after();
+  const int pieces = (p.BN + 31) / 32;
 #pragma unroll 1
-  for (int cc = 0; cc < p.BN / 32; ++cc) {
+  for (int cc = 0; cc < pieces; ++cc) {
     const int cb = n0 + cc * 32;
-    if (cb >= sc_.N || !warp_ok || (kempty && accum)) break;  // warp-uniform
+    if (!warp_ok || (kempty && accum)) break;  // warp-uniform
+    const bool half = p.BN - cc * 32 == 16;    // the tile's last 16 columns
     uint32_t r[32];
     if (kempty) {
 #pragma unroll
@@ -636,15 +642,28 @@ __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, co
     float* buf = stage_buf + (piece & 1u) * DW_PIECE_FLOATS;
     if (lane == 0) bulk_wait_group_read<1>();  // the copy from this buffer two pieces ago is done
     __syncwarp();
+    float4* b4 = reinterpret_cast<float4*>(buf);
+    if (!half) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) buf[j * 32 + lane] = __uint_as_float(r[j]);  // [v][m] rows of 128 B
+      for (int j = 0; j < 8; ++j)  // row `lane`, 16-byte chunk j, 128-byte swizzle
+        b4[lane * 8 + (j ^ (lane & 7))] =
+            make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
+                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)  // rows of 64 bytes, no swizzle
+        b4[lane * 4 + j] =
+            make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
+                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+    }
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
+      const CUtensorMap* map = half ? tmD : tmC;
       if (accum)
-        tma_reduce_add_2d(tmC, buf, mw, cb);
+        tma_reduce_add_2d(map, buf, cb, vw);
       else
-        tma_store_2d(tmC, buf, mw, cb);
+        tma_store_2d(map, buf, cb, vw);
       bulk_commit_group();
     }
     ++piece;
@@ -758,7 +777,8 @@ template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     kd_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -810,14 +830,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int lt = 0;
     uint32_t piece = 0;
     float* my_stage = epi_stage + q * 2 * DW_PIECE_FLOATS;
-    if (MODE == EPI_DW && lane == 0) tma_prefetch_desc(&tmC);
+    if (MODE == EPI_DW && lane == 0) {
+      tma_prefetch_desc(&tmC);
+      tma_prefetch_desc(&tmD);
+    }
     for (int t = blockIdx.x; t < sc.num_tiles; t += gridDim.x, ++lt) {
       const TileCoord c = decode_tile(p, sc, t);
       const int acc = lt & 1;
       const uint32_t use = static_cast<uint32_t>(lt >> 1);
       if (MODE == EPI_DW)
-        epi_dw(p, sc, c, acc, tmem_row, q, tfull, tempty, use, abort_flag, ok, &tmC, my_stage,
-               piece);
+        epi_dw(p, sc, c, acc, tmem_row, q, tfull, tempty, use, abort_flag, ok, &tmC, &tmD,
+               my_stage, piece);
       else if (MODE == EPI_FWD)
         epi_fwd(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else if (MODE == EPI_DZ)
@@ -1054,6 +1077,35 @@ __global__ void kd_gather_rows_kernel(const uint4* __restrict__ h, const int* __
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (r < rows) v = h[static_cast<int64_t>(rowmap[c0 + r]) * d8 + j];
     hc[i] = v;
+  }
+}
+
+// The chunk's valid rows of h, transposed: hcT[j * ld + i] = h[rowmap[c0 + i]][j]
+// for i < rows and 0 for rows <= i < cap, rows = clamp(*nvalid - c0, 0, cap).
+// 32 x 32 tiles through shared memory; block (32, 8).
+__global__ void kd_gather_rows_t_kernel(const __nv_bfloat16* __restrict__ h,
+                                        const int* __restrict__ rowmap,
+                                        const int* __restrict__ nvalid, int c0, int cap, int ld,
+                                        int d, __nv_bfloat16* __restrict__ hcT) {
+  __shared__ __nv_bfloat16 tile[32][33];
+  const int rows = max(0, min(*nvalid - c0, cap));
+  const int j0 = blockIdx.x * 32;
+  const int i0 = blockIdx.y * 32;
+  const int tx = threadIdx.x, ty = threadIdx.y;
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = i0 + ty + 8 * r;
+    const int j = j0 + tx;
+    __nv_bfloat16 v = __float2bfloat16_rn(0.f);
+    if (i < rows && j < d) v = h[static_cast<int64_t>(rowmap[c0 + i]) * d + j];
+    tile[ty + 8 * r][tx] = v;
+  }
+  __syncthreads();
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int j = j0 + ty + 8 * r;
+    const int i = i0 + tx;
+    if (j < d && i < cap) hcT[static_cast<int64_t>(j) * ld + i] = tile[tx][ty + 8 * r];
   }
 }
 
