@@ -243,7 +243,7 @@ template <int MODE>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                 const CUtensorMap& dm, GemmParams p, int sms, cudaStream_t st) {
   if (p.num_tiles <= 0) return KD_OK;
-  p.epi_smem = MODE == EPI_DW ? 4u * 2u * DW_PIECE_FLOATS * 4u : 0u;
+  p.epi_smem = (MODE == EPI_DW || MODE == EPI_DZ) ? 4u * 2u * DW_PIECE_FLOATS * 4u : 0u;
   // the stage ring shares the opt-in shared-memory limit with the staging
   const int fit = static_cast<int>((kMaxDynSmem - 1024u - 256u - p.epi_smem) / p.stage_bytes);
   if (p.stages > fit) p.stages = fit;
@@ -578,7 +578,9 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
     p.dyn_kind = 1;
     p.rowmap = rowmap;
     p.rowmap_base = static_cast<int>(c0);
-    if ((rc = launch_gemm<EPI_DZ>(ta, tb, ta, ta, p, sms, st))) return rc;
+    CUtensorMap tg;  // G chunk as the TMA store target (64-column x 32-row boxes)
+    if (!make_map(&tg, dz, V, C, V, 32)) return KD_ERR_CUDA;
+    if ((rc = launch_gemm<EPI_DZ>(ta, tb, tg, ta, p, sms, st))) return rc;
 
     // (2) dh rows of the chunk, computed transposed: dh_c^T = W^T G_c^T, so a
     // tile is 128 hidden units x 256 chunk rows (A = W as an MN-major operand,

@@ -36,6 +36,7 @@ constexpr int ZBN = 256;           // logit tile width over the vocabulary
 constexpr int TMEM_COLS = 512;     // two accumulators of up to 256 fp32 columns
 constexpr int NUM_THREADS = 192;   // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
 constexpr int MAX_STAGES = 8;
+constexpr int DW_PIECE_FLOATS = 32 * 32;  // one 4 KB epilogue staging buffer (EPI_DZ, EPI_DW)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -394,10 +395,10 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
                                        int acc,
                                        uint32_t tmem_row, int r_in_tile, uint64_t* tfull,
                                        uint64_t* tempty, uint32_t use, volatile int* abort_flag,
-                                       bool& ok) {
+                                       bool& ok, const CUtensorMap* tmC, float* stage_buf,
+                                       uint32_t& piece) {
   const int lrow = c.m * BM + r_in_tile;
-  const bool row_ok = lrow < p.M;      // inside the chunk buffer: always stored
-  const bool active = lrow < sc_.M;    // a real row of this chunk
+  const bool active = lrow < sc_.M;    // a real row of this chunk (others store zeros)
   int64_t grow = 0;
   if (active) grow = p.rowmap ? p.rowmap[p.rowmap_base + lrow] : static_cast<int64_t>(p.row0) + lrow;
   const int v0 = c.n * ZBN;
@@ -426,7 +427,13 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
   ok = __all_sync(0xffffffffu, w);
   if (!ok) return;
   tc_fence_after();
-  __nv_bfloat16* drow = p.dz + static_cast<int64_t>(lrow) * p.dz_ld;
+  // G leaves through the TMA: each warp stages its 32 rows x 64 columns (two
+  // 32-column chunks, 128 bytes of bf16 per row) in the 128-byte swizzle
+  // (chunk j of row r at j ^ (r % 8)) and one lane stores the piece; the TMA
+  // clips rows past the chunk buffer and columns past V.
+  const int lane = threadIdx.x & 31;
+  const int wrow = lrow - lane;  // first row of this warp
+  uint4* b4 = nullptr;
 #pragma unroll 1
   for (int cc = 0; cc < ZBN / 32; ++cc) {
     const int cb = v0 + cc * 32;
@@ -459,22 +466,33 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
         nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
       }
     }
-    if (row_ok) {
+    const int half = cc & 1;
+    if (half == 0) {  // a new 64-column piece: wait until its buffer is free
+      b4 = reinterpret_cast<uint4*>(stage_buf + (piece & 1u) * DW_PIECE_FLOATS);
+      if (lane == 0) bulk_wait_group_read<1>();
+      __syncwarp();
+    }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (cb + 8 * q < p.N) {
-          uint4 pk;
-          __nv_bfloat162 b0 = __floats2bfloat162_rn(g[8 * q + 0], g[8 * q + 1]);
-          __nv_bfloat162 b1 = __floats2bfloat162_rn(g[8 * q + 2], g[8 * q + 3]);
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(g[8 * q + 4], g[8 * q + 5]);
-          __nv_bfloat162 b3 = __floats2bfloat162_rn(g[8 * q + 6], g[8 * q + 7]);
-          pk.x = *reinterpret_cast<uint32_t*>(&b0);
-          pk.y = *reinterpret_cast<uint32_t*>(&b1);
-          pk.z = *reinterpret_cast<uint32_t*>(&b2);
-          pk.w = *reinterpret_cast<uint32_t*>(&b3);
-          *reinterpret_cast<uint4*>(drow + cb + 8 * q) = pk;
-        }
+    for (int q = 0; q < 4; ++q) {
+      uint4 pk;
+      __nv_bfloat162 b0 = __floats2bfloat162_rn(g[8 * q + 0], g[8 * q + 1]);
+      __nv_bfloat162 b1 = __floats2bfloat162_rn(g[8 * q + 2], g[8 * q + 3]);
+      __nv_bfloat162 b2 = __floats2bfloat162_rn(g[8 * q + 4], g[8 * q + 5]);
+      __nv_bfloat162 b3 = __floats2bfloat162_rn(g[8 * q + 6], g[8 * q + 7]);
+      pk.x = *reinterpret_cast<uint32_t*>(&b0);
+      pk.y = *reinterpret_cast<uint32_t*>(&b1);
+      pk.z = *reinterpret_cast<uint32_t*>(&b2);
+      pk.w = *reinterpret_cast<uint32_t*>(&b3);
+      b4[lane * 8 + ((half * 4 + q) ^ (lane & 7))] = pk;
+    }
+    if (half == 1 || cb + 32 >= p.N) {  // piece complete (or the vocabulary ends)
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmC, b4, cb - half * 32, wrow);
+        bulk_commit_group();
       }
+      ++piece;
     }
   }
   tc_fence_before();
@@ -608,8 +626,6 @@ __device__ __forceinline__ void epi_store_t(const GemmParams& p, const Sched& sc
 // Each output element has exactly one owner per launch, so the sum is
 // deterministic.  No barrier spans warps, so a warp that leaves early on an
 // abort cannot leave another waiting.
-constexpr int DW_PIECE_FLOATS = 32 * 32;
-
 __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, const TileCoord& c,
                                        int acc, uint32_t tmem_row, int q, uint64_t* tfull,
                                        uint64_t* tempty, uint32_t use, volatile int* abort_flag,
@@ -844,7 +860,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       else if (MODE == EPI_FWD)
         epi_fwd(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else if (MODE == EPI_DZ)
-        epi_dz(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+        epi_dz(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok, &tmC,
+               my_stage, piece);
       else if (MODE == EPI_STORE)
         epi_store(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else if (MODE == EPI_TMAX)
@@ -856,7 +873,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
     }
     // the TMA copies this warp issued finish before the CTA leaves
-    if (MODE == EPI_DW && lane == 0) bulk_wait_group_all();
+    if ((MODE == EPI_DW || MODE == EPI_DZ) && lane == 0) bulk_wait_group_all();
   }
   tc_fence_before();
   __syncthreads();
