@@ -237,7 +237,7 @@ KERNEL_DESC = {
     "logits_fwd": "forward logit GEMM + online lse + gather",
     "logits_bwd": "backward logit recompute + bf16 gradient tile",
     "dh": "dh^T = W^T G^T over the chunk's valid rows",
-    "dW": "dW^T = h^T G, accumulated over chunks",
+    "dW": "dW = G^T h_c, accumulated over chunks",
 }
 
 
