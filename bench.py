@@ -275,6 +275,7 @@ def run_ours(args, w, world, rank, local_rank):
     torch.cuda.synchronize()
     base_alloc = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
+    free_before = torch.cuda.mem_get_info(dev)[0]  # cross-check with the driver's view
     m = kd.TopKKL(T, V, d, K, chunk, device=dev)
 
     fused = args.api == "fused"
@@ -310,6 +311,7 @@ def run_ours(args, w, world, rank, local_rank):
     torch.cuda.synchronize()
     kd.check_device_status(m.status, "warm-up step")
     peak = torch.cuda.max_memory_allocated(dev)
+    free_after = torch.cuda.mem_get_info(dev)[0]
 
     gpu_id = None
     try:
@@ -414,6 +416,7 @@ def run_ours(args, w, world, rank, local_rank):
                      "traffic": load_traffic(dom)},
         "memory": {"peak_allocated_bytes": int(peak),
                    "peak_minus_inputs_bytes": int(peak - base_alloc),
+                   "device_free_drop_bytes": int(free_before - free_after),
                    "dense_TxV_bf16_bytes": int(T) * int(V) * 2},
         # the fused call runs the teacher prep once instead of twice
         "gpu_launches": int((fl + bl - (1 if fused else 0)) * n),

@@ -129,7 +129,7 @@ Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
   Layout L{};
   size_t off = 0;
   L.nvalid = off;   off += 256;
-  L.losspart = off; off += al256(static_cast<size_t>(cdiv(T, 256)) * 8);
+  L.losspart = off; off += al256(static_cast<size_t>(cdiv(T, 32)) * 8);
   L.sidx = off;     off += al256(static_cast<size_t>(T * K) * 4);
   L.sp = off;       off += al256(static_cast<size_t>(T * K) * 4);
   L.sslot = off;    off += al256(static_cast<size_t>(T * K) * 2);
@@ -501,10 +501,10 @@ int enqueue_forward(const void* h, const void* W, const uint8_t* valid, int64_t 
   p.gidx = gathered_idx;
   if ((rc = launch_gemm<EPI_FWD>(ta, tb, ta, ta, p, sms, st))) return rc;
 
-  const int nb = static_cast<int>(cdiv(T, 256));
-  kd_combine_kernel<<<nb, 256, 0, st>>>(part, p.n_tiles, static_cast<int>(T), K, w.sp, zg,
-                                        w.tterm, var.residual() ? w.resid : nullptr, valid, lse,
-                                        row_kl, var.topk_mass_out, w.losspart);
+  const int nb = static_cast<int>(cdiv(T, 32));
+  kd_combine_kernel<<<nb, dim3(32, COMBINE_SPLIT), 0, st>>>(
+      part, p.n_tiles, static_cast<int>(T), K, w.sp, zg, w.tterm,
+      var.residual() ? w.resid : nullptr, valid, lse, row_kl, var.topk_mass_out, w.losspart);
   kd_loss_final_kernel<<<1, 256, 0, st>>>(w.losspart, nb, w.nvalid, loss);
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }

@@ -963,63 +963,104 @@ __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restr
   }
 }
 
-// One thread per row: lse from the per-tile partials, row_kl, and a per-block
-// (double) partial sum of row_kl for the deterministic loss reduction.
+// lse from the per-tile partials, row_kl, and a per-block (double) partial sum
+// of row_kl for the deterministic loss reduction.  Block (32, COMBINE_SPLIT):
+// thread (x, y) takes row 32 b + x and every COMBINE_SPLIT-th tile (and
+// cached entry) from y, so a warp reads 32 consecutive rows of one tile's
+// partials (coalesced); the COMBINE_SPLIT partial results of a row are merged
+// in the fixed order y = 0, 1, ...
 // resid != null (residual variant): the student mass on the cached entries,
 // s = sum_k exp(zg_k - lse), goes to topk_mass_out (if given) and row_kl gains
 // R (log R - log(1 - s)) for R > 0.
-__global__ void kd_combine_kernel(const float* __restrict__ part, int n_tiles, int T, int K,
-                                  const float* __restrict__ sp, const float* __restrict__ zg,
-                                  const float* __restrict__ tterm,
-                                  const float* __restrict__ resid,
-                                  const uint8_t* __restrict__ valid, float* __restrict__ lse_out,
-                                  float* __restrict__ row_kl_out,
-                                  float* __restrict__ topk_mass_out,
-                                  double* __restrict__ losspart) {
-  __shared__ double red[256];
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  double kl = 0.0;
-  if (row < T) {
-    float m = -CUDART_INF_F;
-    float s = 0.f;
-    for (int j = 0; j < n_tiles; ++j) {
-      const float x = part[static_cast<int64_t>(j) * T + row];
-      if (x > m) {
-        s = s * expf(m - x) + 1.f;
-        m = x;
+constexpr int COMBINE_SPLIT = 8;
+
+__global__ void __launch_bounds__(32 * COMBINE_SPLIT)
+    kd_combine_kernel(const float* __restrict__ part, int n_tiles, int T, int K,
+                      const float* __restrict__ sp, const float* __restrict__ zg,
+                      const float* __restrict__ tterm, const float* __restrict__ resid,
+                      const uint8_t* __restrict__ valid, float* __restrict__ lse_out,
+                      float* __restrict__ row_kl_out, float* __restrict__ topk_mass_out,
+                      double* __restrict__ losspart) {
+  __shared__ float sm[COMBINE_SPLIT][32], ss[COMBINE_SPLIT][32];
+  __shared__ float s_lse[32];
+  __shared__ float sa[COMBINE_SPLIT][32], smass[COMBINE_SPLIT][32];
+  __shared__ double red[32];
+  const int x = threadIdx.x, y = threadIdx.y;
+  const int row = blockIdx.x * 32 + x;
+  const bool in = row < T;
+  // online logsumexp over this thread's tiles
+  float m = -CUDART_INF_F;
+  float s = 0.f;
+  if (in) {
+    for (int j = y; j < n_tiles; j += COMBINE_SPLIT) {
+      const float v = part[static_cast<int64_t>(j) * T + row];
+      if (v > m) {
+        s = s * expf(m - v) + 1.f;
+        m = v;
       } else {
-        s += expf(x - m);
+        s += expf(v - m);
       }
     }
-    const float lse = m + logf(s);
-    if (lse_out) lse_out[row] = lse;
+  }
+  sm[y][x] = m;
+  ss[y][x] = s;
+  __syncthreads();
+  if (y == 0) {
+    float M = sm[0][x], S = ss[0][x];
+    for (int i = 1; i < COMBINE_SPLIT; ++i) {
+      const float mi = sm[i][x], si = ss[i][x];
+      const float mn = fmaxf(M, mi);
+      if (mn != -CUDART_INF_F) S = S * expf(M - mn) + si * expf(mi - mn);
+      M = mn;
+    }
+    const float lse = M + logf(S);
+    s_lse[x] = lse;
+    if (in && lse_out) lse_out[row] = lse;
+  }
+  __syncthreads();
+  const float lse = s_lse[x];
+  // this thread's share of sum_k p_k (lse - zg_k) and of sum_k exp(zg_k - lse)
+  float acc = 0.f, mass = 0.f;
+  if (in) {
     const float* pr = sp + static_cast<int64_t>(row) * K;
     const float* zr = zg + static_cast<int64_t>(row) * K;
-    float mass = 0.f;
-    if (resid) {
-      for (int k = 0; k < K; ++k) mass += expf(zr[k] - lse);
-      if (topk_mass_out) topk_mass_out[row] = mass;
+    for (int k = y; k < K; k += COMBINE_SPLIT) {
+      const float zk = zr[k];
+      acc += pr[k] * (lse - zk);
+      if (resid) mass += expf(zk - lse);
     }
-    float rk = 0.f;
-    if (valid[row]) {
-      float a = 0.f;
-      for (int k = 0; k < K; ++k) a += pr[k] * (lse - zr[k]);
-      rk = tterm[row] + a;
-      if (resid) {
-        const float R = resid[row];
-        if (R > 0.f) rk += R * (logf(R) - log1pf(-mass));
-      }
-    }
-    if (row_kl_out) row_kl_out[row] = rk;
-    kl = rk;
   }
-  red[threadIdx.x] = kl;
+  sa[y][x] = acc;
+  smass[y][x] = mass;
   __syncthreads();
-  for (int o = blockDim.x >> 1; o > 0; o >>= 1) {
-    if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
-    __syncthreads();
+  if (y == 0) {
+    double kl = 0.0;
+    if (in) {
+      float a = 0.f, ms = 0.f;
+      for (int i = 0; i < COMBINE_SPLIT; ++i) {
+        a += sa[i][x];
+        ms += smass[i][x];
+      }
+      if (resid && topk_mass_out) topk_mass_out[row] = ms;
+      float rk = 0.f;
+      if (valid[row]) {
+        rk = tterm[row] + a;
+        if (resid) {
+          const float R = resid[row];
+          if (R > 0.f) rk += R * (logf(R) - log1pf(-ms));
+        }
+      }
+      if (row_kl_out) row_kl_out[row] = rk;
+      kl = rk;
+    }
+    red[x] = kl;
   }
-  if (threadIdx.x == 0) losspart[blockIdx.x] = red[0];
+  __syncthreads();
+  if (y == 0 && x == 0) {
+    double t = 0.0;
+    for (int i = 0; i < 32; ++i) t += red[i];
+    losspart[blockIdx.x] = t;
+  }
 }
 
 // Single block: fixed-order sum of the per-block partials, divided by N_valid.
