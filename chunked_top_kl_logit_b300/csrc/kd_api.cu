@@ -237,6 +237,20 @@ int timing_slot(int kind) {
   return t.used++;
 }
 
+// Opt a kernel into the full dynamic shared-memory limit once per device (a
+// function attribute, not a stream operation: keeping it out of the launch
+// path lets the calls be captured in a CUDA graph).
+template <typename Kernel>
+bool ensure_smem_attr(Kernel kernel, std::once_flag* flags, bool* ok) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  std::call_once(flags[dev], [&] {
+    ok[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(kMaxDynSmem)) == cudaSuccess;
+  });
+  return ok[dev];
+}
+
 // `c` / `dm` are the output tensor maps of EPI_DW (32- and 16-column pieces;
 // ignored by the other modes).
 template <int MODE>
@@ -248,9 +262,9 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c
   const int fit = static_cast<int>((kMaxDynSmem - 1024u - 256u - p.epi_smem) / p.stage_bytes);
   if (p.stages > fit) p.stages = fit;
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + p.epi_smem + 256;
-  if (cudaFuncSetAttribute(kd_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return KD_ERR_CUDA;
+  static std::once_flag attr_once[64];
+  static bool attr_ok[64];
+  if (!ensure_smem_attr(kd_gemm_kernel<MODE>, attr_once, attr_ok)) return KD_ERR_CUDA;
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
   const int slot = MODE == EPI_STORE ? -1 : timing_slot(MODE);
   if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
@@ -267,9 +281,9 @@ int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const GemmParams& p,
                 cudaStream_t st) {
   if (p.num_tiles <= 0) return KD_OK;
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + 256;
-  if (cudaFuncSetAttribute(kd_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return KD_ERR_CUDA;
+  static std::once_flag attr_once[64];
+  static bool attr_ok[64];
+  if (!ensure_smem_attr(kd_gemm_pair_kernel, attr_once, attr_ok)) return KD_ERR_CUDA;
   const int clusters = p.num_tiles < sms / 2 ? p.num_tiles : sms / 2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);

@@ -46,6 +46,11 @@
  *    stream.  Outputs are unspecified when it is nonzero.  The kernels never
  *    trap.
  *  - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - kd_topk_kl_forward, kd_topk_kl_backward and kd_topk_kl_forward_backward
+ *    only enqueue stream-ordered work and never synchronise the host, so a
+ *    sequence of them can be captured in a CUDA graph and replayed, once each
+ *    kernel involved has run on the device (its first use sets a function
+ *    attribute, which is done outside capture).
  */
 #ifndef KD_TOPK_KL_H_
 #define KD_TOPK_KL_H_
