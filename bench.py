@@ -348,7 +348,7 @@ def run_ours(args, w, world, rank, local_rank):
     torch.cuda.synchronize()
     base_alloc = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
-    free_before = torch.cuda.mem_get_info(dev)[0]  # cross-check with the driver's view
+    free_before = torch.cuda.mem_get_info(dev)[0]  # cross-check with the CUDA device's free-memory count
     m = kd.TopKKL(T, V, d, K, chunk, device=dev)
 
     fused = args.api == "fused"
