@@ -98,6 +98,23 @@ def test_teacher_equals_student_is_zero():
     np.testing.assert_array_equal(gpu["gathered_idx"], perm.numpy())
 
 
+def test_teacher_covers_whole_vocabulary():
+    """K = V = 1000 over four vocabulary tiles (the last one ragged): every
+    tile holds 256 cached entries per row, the most the gather and scatter
+    walks ever see, and the top-K softmax is the full-vocabulary one."""
+    g = torch.Generator().manual_seed(17)
+    T, d, V = 150, 128, 1000
+    x = make_inputs(workload("small_4k", T=T, d=d, V=V, K=8, tau=1.25, idx_kind="uniform"))
+    x["teacher_idx"] = torch.stack([torch.randperm(V, generator=g) for _ in range(T)]).to(torch.int32)
+    x["teacher_logits"] = (2.0 * torch.randn(T, V, generator=g)).float()
+    gpu = run_gpu(x, 64)
+    ref = oracle_all(x)
+    assert_forward_parity(gpu, ref)
+    assert rel_l2(gpu["dh"], ref["dh"]) <= GRAD_RL2
+    assert rel_l2(gpu["dW"], ref["dW"]) <= GRAD_RL2
+    np.testing.assert_array_equal(gpu["gathered_idx"], x["teacher_idx"].numpy())
+
+
 def test_duplicate_indices():
     x = make_inputs(workload("small_4k", T=200, d=128, V=1024, K=32, tau=1.0, idx_kind="uniform"))
     idx = x["teacher_idx"].clone()
