@@ -475,8 +475,10 @@ def run_ours(args, w, world, rank, local_rank):
 def run_teacher_topk(args, w, world, rank, local_rank):
     """The teacher-side top-K cache producer on the workload's shape (h, W of a
     synthetic teacher): one step = one kd_teacher_topk call over all T rows
-    (two logit passes per row chunk + selection).  Roofline: tensor, 2 d V
-    FLOPs per row per pass, for the dominant pass (from the library's launch
+    (per row chunk: one logit pass that also stores the chunk's fp32 logits,
+    the threshold, a candidate scan of the stored logits, the selection).
+    Roofline of the logit pass: tensor, 2 d V FLOPs per row; the scan is
+    reported against HBM, 4 V bytes read per row (from the library's launch
     events)."""
     import chunked_top_kl_logit_b300 as kd
     from synth import make_inputs
@@ -522,12 +524,14 @@ def run_teacher_topk(args, w, world, rank, local_rank):
     max_sec = max_over_ranks(ms / 1e3, world, device=dev)
     peaks, src = load_peaks()
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    kern = {}
-    for name, (cnt, kms) in passes.items():
-        fl = 2.0 * T * d * V * n
-        kern[name] = {"launches": cnt, "ms_per_step": kms / n,
-                      "tflops": fl / (kms / 1e3) / 1e12 if kms > 0 else None}
-    dom = max(kern, key=lambda k: kern[k]["ms_per_step"])
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    cnt, kms = passes["topk_pass1"]
+    kern = {"topk_pass1": {"launches": cnt, "ms_per_step": kms / n,
+                           "tflops": 2.0 * T * d * V * n / (kms / 1e3) / 1e12 if kms > 0 else None}}
+    cnt, kms = passes["topk_scan"]
+    scan_gbs = 4.0 * T * V * n / (kms / 1e3) / 1e9 if kms > 0 else None
+    kern["topk_scan"] = {"launches": cnt, "ms_per_step": kms / n, "gbs": scan_gbs,
+                         "hbm_frac": scan_gbs / hbm if scan_gbs else None}
     return {
         "metric": "teacher top-K cache producer rows/s", "op": "teacher_topk",
         "value": job_throughput(T * n, world, max_sec), "unit": "rows/s", "n_gpus": world,
@@ -536,11 +540,12 @@ def run_teacher_topk(args, w, world, rank, local_rank):
         "data": "synthetic",
         "config": {"workload": w.name, "T": T, "V": V, "d": d, "K": K, "tau": w.tau,
                    "chunk": chunk, "l2": "inputs larger than L2 (W alone is V*d*2 B)"},
-        "tflops_two_passes": 4.0 * T * d * V / (max_sec / n) / 1e12,
+        "tflops_logits": 2.0 * T * d * V / (max_sec / n) / 1e12,
         "kernels": kern,
-        "roofline": {"kernel": f"kd_gemm_kernel<{kd.PRODUCER_KERNELS[dom]}> ({dom})",
-                     "bound": "tensor", "achieved": kern[dom]["tflops"], "peak": sustained,
-                     "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / sustained,
+        "roofline": {"kernel": "kd_gemm_kernel<5> (topk_pass1)",
+                     "bound": "tensor", "achieved": kern["topk_pass1"]["tflops"],
+                     "peak": sustained, "unit": "TFLOP/s",
+                     "frac": kern["topk_pass1"]["tflops"] / sustained,
                      "peak_kind": f"bf16 sustained, {src}", "traffic": None},
         "clocks": clocks,
         "gpu_launches": 4 * chunks * n,

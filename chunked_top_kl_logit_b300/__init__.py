@@ -38,7 +38,7 @@ __all__ = [
 
 # contraction kernel ids of the diagnostic timing interface
 KERNELS = {"logits_fwd": 0, "logits_bwd": 1, "dh": 3, "dW": 4}
-PRODUCER_KERNELS = {"topk_pass1": 5, "topk_pass2": 6}
+PRODUCER_KERNELS = {"topk_pass1": 5, "topk_scan": 6}
 
 KD_OK = 0
 KD_ACCUMULATE_DW = 1

@@ -194,8 +194,7 @@ static_assert(static_cast<int>(KD_KERNEL_LOGITS_FWD) == EPI_FWD &&
                   static_cast<int>(KD_KERNEL_LOGITS_BWD) == EPI_DZ &&
                   static_cast<int>(KD_KERNEL_DH) == EPI_DH &&
                   static_cast<int>(KD_KERNEL_DW) == EPI_DW &&
-                  static_cast<int>(KD_KERNEL_TOPK_PASS1) == EPI_TMAX &&
-                  static_cast<int>(KD_KERNEL_TOPK_PASS2) == EPI_TCAND,
+                  static_cast<int>(KD_KERNEL_TOPK_PASS1) == EPI_TMAX,
               "kernel ids of the timing interface follow the epilogue modes");
 
 // Diagnostic launch timing (kd_timing_*): while recording, each contraction
@@ -257,7 +256,9 @@ template <int MODE>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                 const CUtensorMap& dm, GemmParams p, int sms, cudaStream_t st) {
   if (p.num_tiles <= 0) return KD_OK;
-  p.epi_smem = (MODE == EPI_DW || MODE == EPI_DZ) ? 4u * 2u * DW_PIECE_FLOATS * 4u : 0u;
+  p.epi_smem = (MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX)
+                   ? 4u * 2u * DW_PIECE_FLOATS * 4u
+                   : 0u;
   // the stage ring shares the opt-in shared-memory limit with the staging
   const int fit = static_cast<int>((kMaxDynSmem - 1024u - 256u - p.epi_smem) / p.stage_bytes);
   if (p.stages > fit) p.stages = fit;
@@ -378,7 +379,7 @@ void logit_schedule(GemmParams& p, int64_t rows, int64_t V, int64_t d) {
 
 // Workspace of the teacher top-K producer, for chunks of C rows.
 struct TopkLayout {
-  size_t part, tkeys, theta, theta_val, cnt, cand, total;
+  size_t part, tkeys, theta, theta_val, cnt, cand, z, total;
   int64_t C;
   int n_tiles, cap;
 };
@@ -398,6 +399,7 @@ TopkLayout make_topk_layout(int64_t T, int64_t V, int32_t K, int64_t chunk) {
   L.theta_val = off; off += al256(static_cast<size_t>(L.C) * 4);
   L.cnt = off;       off += al256(static_cast<size_t>(L.C) * 4);
   L.cand = off;      off += al256(static_cast<size_t>(L.C) * L.cap * 8);
+  L.z = off;         off += al256(static_cast<size_t>(L.C) * V * 4);  // the chunk's fp32 logits
   L.total = off;
   return L;
 }
@@ -1004,14 +1006,17 @@ int kd_teacher_topk(const void* h, const void* W, int64_t T, int64_t V, int64_t 
   float* theta_val = reinterpret_cast<float*>(wb + L.theta_val);
   int* cnt = reinterpret_cast<int*>(wb + L.cnt);
   uint64_t* cand = reinterpret_cast<uint64_t*>(wb + L.cand);
+  float* z = reinterpret_cast<float*>(wb + L.z);
   if (cudaMemsetAsync(dev_status, 0, sizeof(int32_t), st) != cudaSuccess) return KD_ERR_CUDA;
   const float inv_tau = 1.0f / tau;
   for (int64_t c0 = 0; c0 < T; c0 += L.C) {
     const int64_t rows = (T - c0) < L.C ? (T - c0) : L.C;
     const void* hc = static_cast<const __nv_bfloat16*>(h) + c0 * d;
-    CUtensorMap ta, tb;
-    if (!make_map(&ta, hc, d, rows, d, BM) || !make_map(&tb, W, d, V, d, ZBN)) return KD_ERR_CUDA;
-    // pass 1: tile maxima and lse partials
+    CUtensorMap ta, tb, tz;
+    if (!make_map(&ta, hc, d, rows, d, BM) || !make_map(&tb, W, d, V, d, ZBN) ||
+        !make_map_f32(&tz, z, V, rows, V, 32, 32, true))
+      return KD_ERR_CUDA;
+    // the contraction: tile maxima, lse partials, and the logits into z
     GemmParams p = base_params(0, 0, ZBN);
     logit_schedule(p, rows, V, d);
     p.status = dev_status;
@@ -1020,23 +1025,23 @@ int kd_teacher_topk(const void* h, const void* W, int64_t T, int64_t V, int64_t 
     p.part = part;
     p.part_ld = rows;
     p.tkeys = tkeys;
-    if ((rc = launch_gemm<EPI_TMAX>(ta, tb, ta, ta, p, sms, st))) return rc;
+    if ((rc = launch_gemm<EPI_TMAX>(ta, tb, tz, ta, p, sms, st))) return rc;
     const unsigned blocks = static_cast<unsigned>(cdiv(rows, TOPK_WARPS));
     kd_topk_threshold_kernel<<<blocks, 32 * TOPK_WARPS, 0, st>>>(
         tkeys, part, rows, static_cast<int>(rows), L.n_tiles, K, theta, theta_val,
         full_lse ? full_lse + c0 : nullptr);
     if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(rows) * 4, st) != cudaSuccess)
       return KD_ERR_CUDA;
-    // pass 2: candidates at or above the threshold
-    GemmParams q = base_params(0, 0, ZBN);
-    logit_schedule(q, rows, V, d);
-    q.status = dev_status;
-    q.theta = theta;
-    q.theta_val = theta_val;
-    q.cand = cand;
-    q.cand_cnt = cnt;
-    q.cand_cap = L.cap;
-    if ((rc = launch_gemm<EPI_TCAND>(ta, tb, ta, ta, q, sms, st))) return rc;
+    // candidates at or above the threshold, from the stored logits
+    const int slot = timing_slot(KD_KERNEL_TOPK_SCAN);
+    if (slot >= 0 &&
+        cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
+      return KD_ERR_CUDA;
+    kd_topk_scan_kernel<<<static_cast<unsigned>(rows), SCAN_THREADS, 0, st>>>(
+        z, V, static_cast<int>(V), theta, theta_val, cand, cnt, L.cap, dev_status);
+    if (slot >= 0 &&
+        cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
+      return KD_ERR_CUDA;
     kd_topk_finalize_kernel<<<blocks, 32 * TOPK_WARPS, 0, st>>>(
         cand, cnt, L.cap, static_cast<int>(rows), K, topk_idx + c0 * K, topk_logits + c0 * K);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;

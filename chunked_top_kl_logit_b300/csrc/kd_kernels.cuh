@@ -13,8 +13,9 @@
 //                                             valid-row map (split over V on demand)
 //             dW^T  += h_c^T G_c           -> EPI_DW: TMA store / reduce-add of
 //                                             staged 32 x 32 pieces
-//   teacher   z = h_t W_t^T, two passes    -> EPI_TMAX (tile maxima, lse partials)
-//                                             and EPI_TCAND (candidates)
+//   teacher   z = h_t W_t^T                -> EPI_TMAX: tile maxima, lse partials and
+//                                             the fp32 logits of the chunk (TMA store
+//                                             of staged 32 x 32 pieces)
 //   (diagnostic C = A B^T                  -> EPI_STORE)
 //
 // Warp roles (192 threads): warp 0 issues TMA loads into a ring of shared
@@ -45,15 +46,14 @@ constexpr float LN2 = 0.6931471805599453f;
 // so the stores run along d and coalesce) and written through the row map /
 // accumulated; they differ only in schedule, and are separate instantiations
 // so that profiles tell them apart.
-// EPI_TMAX / EPI_TCAND: the two passes of the teacher-side top-K producer.
+// EPI_TMAX: the contraction of the teacher-side top-K producer.
 enum EpiMode {
   EPI_FWD = 0,
   EPI_DZ = 1,
   EPI_STORE = 2,
   EPI_DH = 3,
   EPI_DW = 4,
-  EPI_TMAX = 5,
-  EPI_TCAND = 6
+  EPI_TMAX = 5
 };
 
 struct GemmParams {
@@ -67,7 +67,7 @@ struct GemmParams {
   int a_mn, b_mn;     // 0: K-major tile, 1: MN-major tile
   int BN;             // tile width (MMA N)
   int stages;
-  uint32_t epi_smem;  // shared-memory bytes of the epilogue's staging buffers (EPI_DW)
+  uint32_t epi_smem;  // shared-memory bytes of the epilogue's staging buffers
   uint32_t a_bytes, b_bytes, stage_bytes;
   uint32_t idesc;
   // epilogue, all modes
@@ -114,16 +114,10 @@ struct GemmParams {
   // {S, n_tiles*BN} in split_info for the reduction that follows.
   int part_rows, policy_sms;
   int* split_info;
-  // Teacher top-K producer (per row of the launch): pass 1 writes the key of
-  // each vocabulary tile's largest logit to tkeys[row * n_tiles + tile]; pass 2
-  // appends every key >= theta[row] to cand[row * cand_cap + ...], counting in
-  // cand_cnt[row].
+  // Teacher top-K producer (per row of the launch): the key of each vocabulary
+  // tile's largest logit goes to tkeys[row * n_tiles + tile]; the logits
+  // themselves leave through the output tensor map (rows x vocabulary, fp32).
   uint64_t* tkeys;
-  const uint64_t* theta;
-  const float* theta_val;
-  uint64_t* cand;
-  int* cand_cnt;
-  int cand_cap;
 };
 
 // Per-launch schedule, resolved on the device at kernel start.
@@ -688,16 +682,23 @@ __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, co
   mbar_arrive(&tempty[acc]);
 }
 
-// Teacher top-K producer, pass 1 (EPI_TMAX): per (row, vocabulary tile) the
-// key of the tile's largest logit (the lowest index among equal maxima) and
-// the natural-log lse partial of z / tau (for the teacher's full-vocabulary
-// normaliser).
+// Teacher top-K producer (EPI_TMAX): per (row, vocabulary tile) the key of
+// the tile's largest logit (the lowest index among equal maxima) and the
+// natural-log lse partial of z / tau (for the teacher's full-vocabulary
+// normaliser); the tile's fp32 logits go out through the TMA (32 x 32 pieces
+// staged in the 128-byte swizzle, columns past the vocabulary clipped) for the
+// candidate scan that follows.
 __device__ __forceinline__ void epi_tmax(const GemmParams& p, const Sched& sc_, const TileCoord& c,
                                          int acc, uint32_t tmem_row, int r_in_tile,
                                          uint64_t* tfull, uint64_t* tempty, uint32_t use,
-                                         volatile int* abort_flag, bool& ok) {
+                                         volatile int* abort_flag, bool& ok,
+                                         const CUtensorMap* tmC, float* stage_buf,
+                                         uint32_t& piece) {
+  const int lane = threadIdx.x & 31;
   const int lrow = c.m * BM + r_in_tile;
   const bool row_ok = lrow < sc_.M;
+  const int wrow = lrow - lane;           // first row of this warp
+  const bool warp_ok = wrow < sc_.M;      // rows past the chunk are clipped by the TMA
   const int v0 = c.n * ZBN;
   bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
   ok = __all_sync(0xffffffffu, w);
@@ -714,6 +715,24 @@ __device__ __forceinline__ void epi_tmax(const GemmParams& p, const Sched& sc_, 
     uint32_t r[32];
     tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
     tmem_ld_wait(r);
+    if (warp_ok) {  // warp-uniform
+      float* buf = stage_buf + (piece & 1u) * DW_PIECE_FLOATS;
+      if (lane == 0) bulk_wait_group_read<1>();  // the copy from this buffer two pieces ago is done
+      __syncwarp();
+      float4* b4 = reinterpret_cast<float4*>(buf);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)  // row `lane`, 16-byte chunk j, 128-byte swizzle
+        b4[lane * 8 + (j ^ (lane & 7))] =
+            make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
+                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmC, buf, cb, wrow);
+        bulk_commit_group();
+      }
+      ++piece;
+    }
     float u[32];
     float cm = -CUDART_INF_F;
 #pragma unroll
@@ -742,51 +761,6 @@ __device__ __forceinline__ void epi_tmax(const GemmParams& p, const Sched& sc_, 
   }
 }
 
-// Teacher top-K producer, pass 2 (EPI_TCAND): every logit whose key is at
-// least the row's threshold becomes a candidate.
-__device__ __forceinline__ void epi_tcand(const GemmParams& p, const Sched& sc_, const TileCoord& c,
-                                          int acc, uint32_t tmem_row, int r_in_tile,
-                                          uint64_t* tfull, uint64_t* tempty, uint32_t use,
-                                          volatile int* abort_flag, bool& ok) {
-  const int lrow = c.m * BM + r_in_tile;
-  const bool row_ok = lrow < sc_.M;
-  const int v0 = c.n * ZBN;
-  uint64_t th = ~0ull;
-  float tv = CUDART_INF_F;
-  if (row_ok) {
-    th = p.theta[lrow];
-    tv = p.theta_val[lrow];
-  }
-  bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
-  ok = __all_sync(0xffffffffu, w);
-  if (!ok) return;
-  tc_fence_after();
-#pragma unroll 1
-  for (int cc = 0; cc < ZBN / 32; ++cc) {
-    const int cb = v0 + cc * 32;
-    if (cb >= p.N) break;
-    uint32_t r[32];
-    tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
-    tmem_ld_wait(r);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float x = __uint_as_float(r[j]);
-      if (x >= tv && cb + j < p.N) {  // rare: only near the row's top-K
-        const uint64_t key = logit_key(x, cb + j);
-        if (key >= th) {
-          const int pos = atomicAdd(p.cand_cnt + lrow, 1);
-          if (pos < p.cand_cap)
-            p.cand[static_cast<int64_t>(lrow) * p.cand_cap + pos] = key;
-          else
-            set_status(p.status, KD_ERR_INTERNAL);
-        }
-      }
-    }
-  }
-  tc_fence_before();
-  mbar_arrive(&tempty[acc]);
-}
-
 // ------------------------------------------------------------------ kernel
 
 template <int MODE>
@@ -798,7 +772,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  // [pipeline stages][epilogue staging (EPI_DW)][barriers, TMEM slot, abort flag]
+  // [pipeline stages][epilogue staging (EPI_DW, EPI_DZ, EPI_TMAX)][barriers, TMEM slot, abort flag]
   float* epi_stage = reinterpret_cast<float*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes +
                                                p.epi_smem);
@@ -865,15 +839,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       else if (MODE == EPI_STORE)
         epi_store(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       else if (MODE == EPI_TMAX)
-        epi_tmax(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
-      else if (MODE == EPI_TCAND)
-        epi_tcand(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+        epi_tmax(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok, &tmC,
+                 my_stage, piece);
       else
         epi_store_t(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
       if (!ok) break;
     }
     // the TMA copies this warp issued finish before the CTA leaves
-    if ((MODE == EPI_DW || MODE == EPI_DZ) && lane == 0) bulk_wait_group_all();
+    if ((MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX) && lane == 0)
+      bulk_wait_group_all();
   }
   tc_fence_before();
   __syncthreads();

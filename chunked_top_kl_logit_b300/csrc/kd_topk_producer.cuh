@@ -1,17 +1,18 @@
-// Teacher-side top-K cache producer: the SIMT steps between and after the two
-// contraction passes (aipuls.nl summary of "Making Knowledge Distillation
-// Cheap Enough to Run at Scale", section "Summary": the teacher's top-100
-// logits per position are cached offline).
+// Teacher-side top-K cache producer: the SIMT steps after the contraction
+// (aipuls.nl summary of "Making Knowledge Distillation Cheap Enough to Run at
+// Scale", section "Summary": the teacher's top-100 logits per position are
+// cached offline).
 //
 // Every logit z_tv gets the unique 64-bit key (order(z), ~v): larger logit
-// first, then the lower vocabulary index.  Pass 1 (EPI_TMAX) records each
-// vocabulary tile's largest key.  The K-th largest of those tile maxima, theta,
-// is a lower bound of the row's K-th largest key (the K tiles with the largest
-// maxima hold K distinct keys >= theta), and only the fewer than K tiles whose
-// maximum exceeds theta, plus theta itself, can hold keys >= theta: at most
-// (K - 1) * 256 + 1 candidates.  Pass 2 (EPI_TCAND) collects them; the
-// finalize kernel selects the K largest candidate keys exactly and writes them
-// in descending order.
+// first, then the lower vocabulary index.  The contraction (EPI_TMAX) records
+// each vocabulary tile's largest key and stores the chunk's fp32 logits.  The
+// K-th largest of those tile maxima, theta, is a lower bound of the row's K-th
+// largest key (the K tiles with the largest maxima hold K distinct keys >=
+// theta), and only the fewer than K tiles whose maximum exceeds theta, plus
+// theta itself, can hold keys >= theta: at most (K - 1) * 256 + 1 candidates.
+// The scan kernel collects them from the stored logits; the finalize kernel
+// selects the K largest candidate keys exactly and writes them in descending
+// order.
 #pragma once
 
 #include <math_constants.h>
@@ -115,6 +116,53 @@ __global__ void kd_topk_threshold_kernel(const uint64_t* __restrict__ tkeys,
     theta[row] = th;
     theta_val[row] = th ? float_from_order_key(static_cast<uint32_t>(th >> 32)) : -CUDART_INF_F;
     if (full_lse) full_lse[row] = m + logf(s);
+  }
+}
+
+constexpr int SCAN_THREADS = 256;  // one block per row of the chunk
+
+// One block per row: every stored logit whose key is at least the row's
+// threshold becomes a candidate (appended in no particular order; the
+// finalize kernel sorts).  z holds the row's V logits (V a multiple of 8, rows
+// 32-byte aligned); the value test discards almost every logit before a key is
+// formed.
+__global__ void __launch_bounds__(SCAN_THREADS)
+    kd_topk_scan_kernel(const float* __restrict__ z, int64_t ldz, int V,
+                        const uint64_t* __restrict__ theta, const float* __restrict__ theta_val,
+                        uint64_t* __restrict__ cand, int* __restrict__ cand_cnt, int cand_cap,
+                        int* status) {
+  const int row = blockIdx.x;
+  const uint64_t th = theta[row];
+  const float tv = theta_val[row];
+  const float4* z4 = reinterpret_cast<const float4*>(z + static_cast<int64_t>(row) * ldz);
+  const int n4 = V >> 2;
+  constexpr int U = 4;  // independent 16-byte loads in flight per thread
+  for (int base = threadIdx.x; base < n4; base += U * SCAN_THREADS) {
+    float4 q[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * SCAN_THREADS;
+      q[u] = i < n4 ? __ldcs(z4 + i) : make_float4(-CUDART_INF_F, -CUDART_INF_F,
+                                                   -CUDART_INF_F, -CUDART_INF_F);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * SCAN_THREADS;
+      const float xs[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (i < n4 && xs[e] >= tv) {  // rare: only near the row's top-K
+          const uint64_t key = logit_key(xs[e], 4 * i + e);
+          if (key >= th) {
+            const int pos = atomicAdd(cand_cnt + row, 1);
+            if (pos < cand_cap)
+              cand[static_cast<int64_t>(row) * cand_cap + pos] = key;
+            else
+              set_status(status, KD_ERR_INTERNAL);
+          }
+        }
+      }
+    }
   }
 }
 

@@ -213,13 +213,15 @@ int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* te
  *   full_lse    fp32  [T]      log sum_v exp(z_tv / tau), or NULL: the
  *                              teacher_lse that kd_topk_kl_forward_residual takes
  *
- * Two passes of the tensor-core logit GEMM per chunk of `chunk` rows: the first
- * records each 256-column tile's largest logit (and lse partials), a per-row
- * threshold (the K-th largest tile maximum) bounds the candidates to at most
- * (K - 1) * 256 + 1 per row, the second collects them, and an exact selection
- * orders the K largest.  The workspace holds one chunk's candidates:
- * kd_teacher_topk_workspace_size(...) ~ chunk * 8 * min(V, (K - 1) * 256 + 1)
- * bytes.  Inputs must be finite.  Limits and errors as kd_topk_kl_forward
+ * One tensor-core logit GEMM per chunk of `chunk` rows records each
+ * 256-column tile's largest logit and lse partials and stores the chunk's fp32
+ * logits in the workspace; a per-row threshold (the K-th largest tile maximum)
+ * bounds the candidates to at most (K - 1) * 256 + 1 per row, a scan of the
+ * stored logits collects them, and an exact selection orders the K largest.
+ * The workspace holds one chunk's logits and candidates:
+ * kd_teacher_topk_workspace_size(...) ~ chunk * (4 V + 8 min(V, (K - 1) * 256 + 1))
+ * bytes (3.3 GB + 0.8 GB at chunk = 4096, V = 201088, K = 100); a smaller chunk
+ * bounds it.  Inputs must be finite.  Limits and errors as kd_topk_kl_forward
  * (KD_ERR_INTERNAL in *dev_status would mean a candidate bound was exceeded,
  * which the construction rules out).  Deterministic.
  */
@@ -332,7 +334,8 @@ int kd_topk_kl_forward_noalloc(const void* h, const void* W, const int32_t* teac
  *   KD_KERNEL_DH          dh = G W (computed as dh^T = W^T G^T)
  *   KD_KERNEL_DW          dW = G^T h (computed as dW^T = h^T G)
  *   KD_KERNEL_TOPK_PASS1  teacher top-K producer: logits, tile maxima, lse partials
- *   KD_KERNEL_TOPK_PASS2  teacher top-K producer: logits, candidate collection
+ *   KD_KERNEL_TOPK_SCAN   teacher top-K producer: candidate scan of the stored
+ *                         logits (a SIMT kernel, timed the same way)
  *
  * kd_timing_start(capacity): creates 2 x capacity CUDA events on the current
  *   device (no device memory is allocated) and starts recording: from then on
@@ -352,7 +355,7 @@ enum {
   KD_KERNEL_DH = 3,
   KD_KERNEL_DW = 4,
   KD_KERNEL_TOPK_PASS1 = 5,
-  KD_KERNEL_TOPK_PASS2 = 6
+  KD_KERNEL_TOPK_SCAN = 6
 };
 int kd_timing_start(int32_t capacity);
 int kd_timing_stop(void);
