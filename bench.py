@@ -541,6 +541,7 @@ def run_teacher_topk(args, w, world, rank, local_rank):
         "config": {"workload": w.name, "T": T, "V": V, "d": d, "K": K, "tau": w.tau,
                    "chunk": chunk, "l2": "inputs larger than L2 (W alone is V*d*2 B)"},
         "tflops_logits": 2.0 * T * d * V / (max_sec / n) / 1e12,
+        "memory": {"workspace_bytes": int(ws.numel())},
         "kernels": kern,
         "roofline": {"kernel": "kd_gemm_kernel<5> (topk_pass1)",
                      "bound": "tensor", "achieved": kern["topk_pass1"]["tflops"],
