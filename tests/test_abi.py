@@ -175,3 +175,37 @@ def test_residual_entry_argument_checks():
     assert L.kd_topk_kl_backward_residual(vp(A), vp(A), vp(A), vp(A), vp(A), vp(A), T, V, d, K,
                                           1.0, chunk, vp(A), vp(A), 1.0, vp(A), vp(A), vp(A),
                                           b - 1, vp(A), None) == WORKSPACE
+
+
+def test_teacher_topk_workspace_and_argument_checks():
+    """The producer's workspace holds one chunk's fp32 logits (chunk x V x 4 B)
+    and its candidates (at most (K - 1) * 256 + 1 keys of 8 B per row, or the
+    whole row when it has fewer than K vocabulary tiles); bad arguments and a
+    short workspace are rejected before any CUDA call."""
+    T, V, d, K = 32768, 201088, 2880, 100
+    cap = (K - 1) * 256 + 1
+    sizes = [kd.kd_teacher_topk_workspace_size(T, V, d, K, c) for c in (1024, 4096, 8192)]
+    for c, b in zip((1024, 4096, 8192), sizes):
+        assert c * V * 4 + c * cap * 8 <= b < c * V * 4 + c * cap * 8 + c * 786 * 12 + (1 << 22)
+    assert sizes[0] < sizes[1] < sizes[2]
+    # fewer vocabulary tiles than K: every logit of the row is a candidate
+    b = kd.kd_teacher_topk_workspace_size(64, 1024, 64, 8, 64)
+    assert 64 * 1024 * 4 + 64 * 1024 * 8 <= b
+    vp = ctypes.c_void_p
+    L = kd.lib()
+    T, V, d, K, chunk = 64, 1024, 64, 8, 64
+    b = kd.kd_teacher_topk_workspace_size(T, V, d, K, chunk)
+
+    def call(**kw):
+        a = dict(h=A, W=A, tau=1.0, idx=A, val=A, lse=None, ws=A, ws_bytes=b, status=A, d=d, V=V)
+        a.update(kw)
+        return L.kd_teacher_topk(vp(a["h"]), vp(a["W"]), T, a["V"], a["d"], K, a["tau"], chunk,
+                                 vp(a["idx"]), vp(a["val"]), vp(a["lse"]), vp(a["ws"]),
+                                 a["ws_bytes"], vp(a["status"]), None)
+
+    for kw in (dict(h=None), dict(W=None), dict(idx=None), dict(val=None), dict(ws=None),
+               dict(status=None), dict(tau=0.0), dict(tau=float("nan")), dict(h=A + 8),
+               dict(ws=A + 4), dict(idx=A + 2), dict(lse=A + 2)):
+        assert call(**kw) == INVALID, kw
+    assert call(ws_bytes=b - 1) == WORKSPACE
+    assert call(V=1020) == UNSUPPORTED and call(d=96) == UNSUPPORTED
