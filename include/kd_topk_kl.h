@@ -339,8 +339,9 @@ int kd_topk_kl_forward_noalloc(const void* h, const void* W, const int32_t* teac
  *
  * kd_timing_start(capacity): creates 2 x capacity CUDA events on the current
  *   device (no device memory is allocated) and starts recording: from then on
- *   every contraction launch that kd_topk_kl_forward / kd_topk_kl_backward
- *   make (and kd_teacher_topk), from any host thread, is bracketed by an event pair recorded on its
+ *   every launch of an id above that the entry points make (the contractions
+ *   of the loss entries and of kd_teacher_topk, and the producer's candidate
+ *   scan), from any host thread, is bracketed by an event pair recorded on its
  *   stream, until `capacity` launches have been recorded.  Restarting discards
  *   earlier records.
  * kd_timing_stop(): stops recording; the records stay readable.
