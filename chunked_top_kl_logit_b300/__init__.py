@@ -34,6 +34,7 @@ __all__ = [
     "kd_teacher_topk_workspace_size", "kd_teacher_topk", "PRODUCER_KERNELS",
     "kd_gemm_bf16_diag", "kd_gemm_bf16_diag_pair", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
     "KERNELS", "kd_timing_start", "kd_timing_stop", "kd_timing_query", "kd_timing_release",
+    "topk_kl_loss",
 ]
 
 # contraction kernel ids of the diagnostic timing interface
@@ -319,6 +320,67 @@ def check_device_status(dev_status, where: str = "device"):
     code = int(dev_status.item())
     if code != KD_OK:
         raise KDError(code, where)
+
+
+class _TopKKLFunction(torch.autograd.Function):
+    """Autograd adapter: the forward runs kd_topk_kl_forward, the backward
+    kd_topk_kl_backward with the upstream gradient as grad_loss.  Workspaces are
+    allocated per call from torch's caching allocator."""
+
+    @staticmethod
+    def forward(ctx, h, W, teacher_idx, teacher_logits, valid, tau, chunk):
+        T, d = h.shape
+        V = W.shape[0]
+        K = teacher_idx.shape[1]
+        fwd, _ = kd_topk_kl_workspace_size(T, V, d, K, chunk)
+        dev = h.device
+        ws = torch.empty(fwd, dtype=torch.uint8, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        loss = torch.empty(1, dtype=torch.float32, device=dev)
+        lse = torch.empty(T, dtype=torch.float32, device=dev)
+        kd_topk_kl_forward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, loss, lse,
+                           ws=ws, dev_status=status)
+        ctx.save_for_backward(h, W, teacher_idx, teacher_logits, valid, lse, status)
+        ctx.tau, ctx.chunk = float(tau), int(chunk)
+        return loss.view(())
+
+    @staticmethod
+    def backward(ctx, grad):
+        h, W, teacher_idx, teacher_logits, valid, lse, status = ctx.saved_tensors
+        check_device_status(status, "kd_topk_kl_forward")
+        T, d = h.shape
+        V = W.shape[0]
+        K = teacher_idx.shape[1]
+        _, bwd = kd_topk_kl_workspace_size(T, V, d, K, ctx.chunk)
+        ws = torch.empty(bwd, dtype=torch.uint8, device=h.device)
+        dh = torch.empty(T, d, dtype=torch.float32, device=h.device)
+        dW = torch.empty(V, d, dtype=torch.float32, device=h.device)
+        kd_topk_kl_backward(h, W, teacher_idx, teacher_logits, valid, ctx.tau, ctx.chunk, lse,
+                            float(grad), dh, dW, ws=ws, dev_status=status)
+        check_device_status(status, "kd_topk_kl_backward")
+        return dh, dW, None, None, None, None, None
+
+
+def topk_kl_loss(h, W, teacher_idx, teacher_logits, valid, tau, chunk=4096):
+    """The fused top-K KL distillation loss as a differentiable torch function.
+
+    h bf16 [T, d] and W bf16 [V, d] (the student's final hidden states and LM
+    head), teacher_idx int32 [T, K], teacher_logits fp32 [T, K], valid uint8 [T],
+    all contiguous on one CUDA device.  Returns the scalar loss (fp32); its
+    backward gives dh and dW from the library (fp32; autograd casts them to the
+    parameters' dtype).  The backward reads the upstream gradient and the status
+    word on the host (two synchronisations) and raises KDError on a device error.
+    """
+    args = ((h, torch.bfloat16, "h"), (W, torch.bfloat16, "W"),
+            (teacher_idx, torch.int32, "teacher_idx"),
+            (teacher_logits, torch.float32, "teacher_logits"), (valid, torch.uint8, "valid"))
+    for t, dt, name in args:
+        if t.dtype != dt:
+            raise TypeError(f"{name} must be {dt}, got {t.dtype}")
+    for t, _, name in args:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+    return _TopKKLFunction.apply(h, W, teacher_idx, teacher_logits, valid, tau, chunk)
 
 
 class TopKKL:

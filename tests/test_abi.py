@@ -209,3 +209,20 @@ def test_teacher_topk_workspace_and_argument_checks():
         assert call(**kw) == INVALID, kw
     assert call(ws_bytes=b - 1) == WORKSPACE
     assert call(V=1020) == UNSUPPORTED and call(d=96) == UNSUPPORTED
+
+
+def test_autograd_adapter_checks_inputs_before_any_call():
+    """topk_kl_loss rejects wrong dtypes and host tensors before touching the
+    library."""
+    import torch
+    h = torch.zeros(4, 64, dtype=torch.bfloat16)
+    W = torch.zeros(1024, 64, dtype=torch.bfloat16)
+    idx = torch.zeros(4, 2, dtype=torch.int32)
+    tl = torch.zeros(4, 2, dtype=torch.float32)
+    valid = torch.ones(4, dtype=torch.uint8)
+    with pytest.raises(TypeError):
+        kd.topk_kl_loss(h.float(), W, idx, tl, valid, 1.0, 4)
+    with pytest.raises(TypeError):
+        kd.topk_kl_loss(h, W, idx.long(), tl, valid, 1.0, 4)
+    with pytest.raises(ValueError):
+        kd.topk_kl_loss(h, W, idx, tl, valid, 1.0, 4)  # host tensors
