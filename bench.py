@@ -140,11 +140,11 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-DEVICE_SOURCES = ("kd_kernels.cuh", "kd_ptx.cuh")
+DEVICE_SOURCES = ("kd_kernels.cuh", "kd_ptx.cuh", "kd_topk_producer.cuh")
 
 
 def device_source_sha256() -> str:
-    """Hash of the device-code files the GEMM kernel is compiled from."""
+    """Hash of the device-code files the profiled kernels are compiled from."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "chunked_top_kl_logit_b300", "csrc")
@@ -547,7 +547,10 @@ def run_teacher_topk(args, w, world, rank, local_rank):
                      "bound": "tensor", "achieved": kern["topk_pass1"]["tflops"],
                      "peak": sustained, "unit": "TFLOP/s",
                      "frac": kern["topk_pass1"]["tflops"] / sustained,
-                     "peak_kind": f"bf16 sustained, {src}", "traffic": None},
+                     "peak_kind": f"bf16 sustained, {src}",
+                     # measured at ctx_32k shapes with 4096-row chunks only
+                     "traffic": load_traffic("topk_pass1")
+                     if (w.name, chunk) == ("ctx_32k", 4096) else None},
         "clocks": clocks,
         "gpu_launches": 4 * chunks * n,
     }
