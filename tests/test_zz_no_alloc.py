@@ -4,9 +4,10 @@ Some callers cannot call cudaMalloc at all, for example code that runs
 inside another framework's memory manager, which owns the whole device pool.
 For them the library offers a forward whose workspace is a fixed 32 MiB array
 built into the library.  These tests call it through the C ABI and hold it to
-the regular kd_topk_kl_forward (same tolerances as every parity test), on two
-calls in a row with different inputs, so that contents left in the shared
-array by the first call cannot leak into the second.
+the regular kd_topk_kl_forward and to the fp64 oracle (same tolerances as
+every parity test), on two calls in a row with different inputs, so that
+contents left in the shared array by the first call cannot leak into the
+second.
 
 The file is named so that pytest collects it last.
 """
@@ -18,8 +19,9 @@ import pytest
 import torch
 
 import chunked_top_kl_logit_b300 as kd
+from oracle import kd_oracle as O
 from synth import make_inputs, workload
-from tests.gpu_util import LOSS_RTOL, LSE_ATOL, to_device
+from tests.gpu_util import LOSS_RTOL, LSE_ATOL, oracle_inputs, to_device
 
 KD_ERR_SCRATCH_LIMIT = 7
 
@@ -67,4 +69,11 @@ def test_matches_regular_forward_on_two_calls_in_a_row():
         assert np.abs(lse - rlse).max() <= LSE_ATOL
         assert np.abs(row_kl - rrow).max() <= LSE_ATOL
         np.testing.assert_array_equal(gidx, rgidx)
-        np.testing.assert_array_equal(gidx, x["teacher_idx"].numpy())
+        # and the oracle, which shares no code with either kernel path
+        P = oracle_inputs(x)
+        f = O.forward(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], P["valid"],
+                      P["tau"], block=1024)
+        assert abs(loss - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+        assert np.abs(lse - f["lse"]).max() <= LSE_ATOL
+        assert np.abs(row_kl - f["row_kl"]).max() <= LSE_ATOL
+        np.testing.assert_array_equal(gidx, f["gathered_idx"])
