@@ -356,12 +356,12 @@ def run_ours(args, w, world, rank, local_rank):
     if residual:
         from synth import teacher_full_lse
         tlse = teacher_full_lse(x["teacher_logits"].cpu(), tau, seed=args.seed + rank).to(dev)
-        topk_mass = torch.empty(T, dtype=torch.float32, device=dev)
+        outside_mass = torch.empty(T, dtype=torch.float32, device=dev)
 
     def fwd_part():
         if residual:
             kd.kd_topk_kl_forward_residual(h, W, idx, tl, tlse, valid, tau, chunk, m.loss, m.lse,
-                                           m.row_kl, topk_mass, ws=m.ws, dev_status=m.status)
+                                           m.row_kl, outside_mass, ws=m.ws, dev_status=m.status)
         elif fused:
             m.forward_backward(h, W, idx, tl, valid, tau, 1.0)
         else:
@@ -370,7 +370,7 @@ def run_ours(args, w, world, rank, local_rank):
     def bwd_part():
         if residual:
             kd.kd_topk_kl_backward_residual(h, W, idx, tl, tlse, valid, tau, chunk, m.lse,
-                                            topk_mass, 1.0, m.dh, m.dW, ws=m.ws,
+                                            outside_mass, 1.0, m.dh, m.dW, ws=m.ws,
                                             dev_status=m.status)
         elif not fused:
             m.backward(h, W, idx, tl, valid, tau, 1.0)

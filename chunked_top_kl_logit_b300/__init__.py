@@ -133,9 +133,20 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _stream(stream, *tensors):
+    """Handle of the stream the library enqueues on (`stream`, else torch's
+    current stream).  The library takes its launch configuration and tensor
+    maps from the current device, so every tensor and the stream must live on
+    the current device; anything else raises before a call is made."""
+    cur = torch.cuda.current_device()
     if stream is None:
         stream = torch.cuda.current_stream()
+    if stream.device.index != cur:
+        raise ValueError(f"the stream is on {stream.device} but the current device is cuda:{cur}")
+    for t in tensors:
+        if t is not None and (t.device.type != "cuda" or t.device.index != cur):
+            raise ValueError(f"a tensor is on {t.device} but the current device is cuda:{cur}; "
+                             f"run the call inside torch.cuda.device(...) of its tensors")
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -163,10 +174,12 @@ def kd_topk_kl_forward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, los
     T, d = h.shape
     V = W.shape[0]
     K = teacher_idx.shape[1]
+    st = _stream(stream, h, W, teacher_idx, teacher_logits, valid, loss, lse, row_kl,
+                 gathered_idx, ws, dev_status)
     rc = lib().kd_topk_kl_forward(_ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits),
                                   _ptr(valid), T, V, d, K, float(tau), int(chunk), _ptr(loss),
                                   _ptr(lse), _ptr(row_kl), _ptr(gathered_idx), _ptr(ws),
-                                  ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+                                  ws.numel() * ws.element_size(), _ptr(dev_status), st)
     _check(rc, "kd_topk_kl_forward")
 
 
@@ -176,10 +189,12 @@ def kd_topk_kl_forward_noalloc(h, W, teacher_idx, teacher_logits, valid, tau, lo
     T, d = h.shape
     V = W.shape[0]
     K = teacher_idx.shape[1]
+    st = _stream(stream, h, W, teacher_idx, teacher_logits, valid, loss, lse, row_kl,
+                 gathered_idx, dev_status)
     rc = lib().kd_topk_kl_forward_noalloc(_ptr(h), _ptr(W), _ptr(teacher_idx),
                                           _ptr(teacher_logits), _ptr(valid), T, V, d, K,
                                           float(tau), _ptr(loss), _ptr(lse), _ptr(row_kl),
-                                          _ptr(gathered_idx), _ptr(dev_status), _stream(stream))
+                                          _ptr(gathered_idx), _ptr(dev_status), st)
     _check(rc, "kd_topk_kl_forward_noalloc")
 
 
@@ -188,11 +203,11 @@ def kd_topk_kl_backward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, ls
     T, d = h.shape
     V = W.shape[0]
     K = teacher_idx.shape[1]
+    st = _stream(stream, h, W, teacher_idx, teacher_logits, valid, lse, dh, dW, ws, dev_status)
     rc = lib().kd_topk_kl_backward(_ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits),
                                    _ptr(valid), T, V, d, K, float(tau), int(chunk), _ptr(lse),
                                    float(grad_loss), _ptr(dh), _ptr(dW), _ptr(ws),
-                                   ws.numel() * ws.element_size(), _ptr(dev_status),
-                                   _stream(stream))
+                                   ws.numel() * ws.element_size(), _ptr(dev_status), st)
     _check(rc, "kd_topk_kl_backward")
 
 
@@ -203,39 +218,45 @@ def kd_topk_kl_forward_backward(h, W, teacher_idx, teacher_logits, valid, tau, c
     T, d = h.shape
     V = W.shape[0]
     K = teacher_idx.shape[1]
+    st = _stream(stream, h, W, teacher_idx, teacher_logits, valid, loss, lse, row_kl, dh, dW,
+                 ws, dev_status)
     rc = lib().kd_topk_kl_forward_backward(
         _ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits), _ptr(valid), T, V, d, K,
         float(tau), int(chunk), float(grad_loss), int(flags), _ptr(loss), _ptr(lse), _ptr(row_kl),
-        _ptr(dh), _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
-        _stream(stream))
+        _ptr(dh), _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), st)
     _check(rc, "kd_topk_kl_forward_backward")
 
 
 def kd_topk_kl_forward_residual(h, W, teacher_idx, teacher_logits, teacher_lse, valid, tau, chunk,
-                                loss, lse, row_kl=None, topk_mass=None, *, ws, dev_status,
+                                loss, lse, row_kl=None, outside_mass=None, *, ws, dev_status,
                                 stream=None):
-    """Forward of the residual-mass variant (teacher full-vocabulary normaliser)."""
+    """Forward of the residual-mass variant (teacher full-vocabulary normaliser);
+    outside_mass receives the student's mass outside the cached entries."""
     T, d = h.shape
     V = W.shape[0]
     K = teacher_idx.shape[1]
+    st = _stream(stream, h, W, teacher_idx, teacher_logits, teacher_lse, valid, loss, lse,
+                 row_kl, outside_mass, ws, dev_status)
     rc = lib().kd_topk_kl_forward_residual(
         _ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits), _ptr(teacher_lse), _ptr(valid),
-        T, V, d, K, float(tau), int(chunk), _ptr(loss), _ptr(lse), _ptr(row_kl), _ptr(topk_mass),
-        _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+        T, V, d, K, float(tau), int(chunk), _ptr(loss), _ptr(lse), _ptr(row_kl),
+        _ptr(outside_mass), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), st)
     _check(rc, "kd_topk_kl_forward_residual")
 
 
 def kd_topk_kl_backward_residual(h, W, teacher_idx, teacher_logits, teacher_lse, valid, tau,
-                                 chunk, lse, topk_mass, grad_loss, dh, dW, *, ws, dev_status,
+                                 chunk, lse, outside_mass, grad_loss, dh, dW, *, ws, dev_status,
                                  stream=None):
-    """Backward of the residual-mass variant; lse and topk_mass from its forward."""
+    """Backward of the residual-mass variant; lse and outside_mass from its forward."""
     T, d = h.shape
     V = W.shape[0]
     K = teacher_idx.shape[1]
+    st = _stream(stream, h, W, teacher_idx, teacher_logits, teacher_lse, valid, lse,
+                 outside_mass, dh, dW, ws, dev_status)
     rc = lib().kd_topk_kl_backward_residual(
         _ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits), _ptr(teacher_lse), _ptr(valid),
-        T, V, d, K, float(tau), int(chunk), _ptr(lse), _ptr(topk_mass), float(grad_loss), _ptr(dh),
-        _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+        T, V, d, K, float(tau), int(chunk), _ptr(lse), _ptr(outside_mass), float(grad_loss),
+        _ptr(dh), _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), st)
     _check(rc, "kd_topk_kl_backward_residual")
 
 
@@ -252,9 +273,10 @@ def kd_teacher_topk(h, W, K, tau, chunk, topk_idx, topk_logits, full_lse=None, *
     their indices, and optionally the full-vocabulary lse of z / tau."""
     T, d = h.shape
     V = W.shape[0]
+    st = _stream(stream, h, W, topk_idx, topk_logits, full_lse, ws, dev_status)
     rc = lib().kd_teacher_topk(_ptr(h), _ptr(W), T, V, d, int(K), float(tau), int(chunk),
                                _ptr(topk_idx), _ptr(topk_logits), _ptr(full_lse), _ptr(ws),
-                               ws.numel() * ws.element_size(), _ptr(dev_status), _stream(stream))
+                               ws.numel() * ws.element_size(), _ptr(dev_status), st)
     _check(rc, "kd_teacher_topk")
 
 
@@ -269,28 +291,30 @@ def kd_entropy_filter(teacher_logits, valid_in, tau, keep_num, keep_den, valid_o
                       entropy=None, *, ws, dev_status, stream=None):
     """Keep the ceil(N_in * keep_num / keep_den) highest-entropy valid rows."""
     T, K = teacher_logits.shape
+    st = _stream(stream, teacher_logits, valid_in, valid_out, entropy, ws, dev_status)
     rc = lib().kd_entropy_filter(_ptr(teacher_logits), _ptr(valid_in), T, K, float(tau),
                                  int(keep_num), int(keep_den), _ptr(valid_out), _ptr(entropy),
-                                 _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
-                                 _stream(stream))
+                                 _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), st)
     _check(rc, "kd_entropy_filter")
 
 
 def kd_gemm_bf16_diag(A, B, C, M, N, Kd, a_mn, b_mn, *, dev_status, stream=None):
+    st = _stream(stream, A, B, C, dev_status)
     rc = lib().kd_gemm_bf16_diag(_ptr(A), _ptr(B), _ptr(C), M, N, Kd, int(a_mn), int(b_mn),
-                                 _ptr(dev_status), _stream(stream))
+                                 _ptr(dev_status), st)
     _check(rc, "kd_gemm_bf16_diag")
 
 
 def kd_gemm_bf16_diag_pair(A, B, C, M, N, Kd, *, dev_status, stream=None):
     """C = A B^T on the CTA-pair (cta_group::2) pipeline; A [M, Kd], B [N, Kd] bf16."""
-    rc = lib().kd_gemm_bf16_diag_pair(_ptr(A), _ptr(B), _ptr(C), M, N, Kd, _ptr(dev_status),
-                                      _stream(stream))
+    st = _stream(stream, A, B, C, dev_status)
+    rc = lib().kd_gemm_bf16_diag_pair(_ptr(A), _ptr(B), _ptr(C), M, N, Kd, _ptr(dev_status), st)
     _check(rc, "kd_gemm_bf16_diag_pair")
 
 
 def kd_pipeline_wait_selftest(limit_ns, *, dev_status, stream=None):
-    rc = lib().kd_pipeline_wait_selftest(int(limit_ns), _ptr(dev_status), _stream(stream))
+    st = _stream(stream, dev_status)
+    rc = lib().kd_pipeline_wait_selftest(int(limit_ns), _ptr(dev_status), st)
     _check(rc, "kd_pipeline_wait_selftest")
 
 
@@ -347,6 +371,12 @@ class _TopKKLFunction(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad):
         h, W, teacher_idx, teacher_logits, valid, lse, status = ctx.saved_tensors
+        with torch.cuda.device(h.device):
+            return _TopKKLFunction._backward(ctx, grad, h, W, teacher_idx, teacher_logits, valid,
+                                             lse, status)
+
+    @staticmethod
+    def _backward(ctx, grad, h, W, teacher_idx, teacher_logits, valid, lse, status):
         check_device_status(status, "kd_topk_kl_forward")
         T, d = h.shape
         V = W.shape[0]
@@ -366,7 +396,8 @@ def topk_kl_loss(h, W, teacher_idx, teacher_logits, valid, tau, chunk=4096):
 
     h bf16 [T, d] and W bf16 [V, d] (the student's final hidden states and LM
     head), teacher_idx int32 [T, K], teacher_logits fp32 [T, K], valid uint8 [T],
-    all contiguous on one CUDA device.  Returns the scalar loss (fp32); its
+    all contiguous on one CUDA device (checked; the call runs with that device
+    current).  Returns the scalar loss (fp32); its
     backward gives dh and dW from the library (fp32; autograd casts them to the
     parameters' dtype).  The backward reads the upstream gradient and the status
     word on the host (two synchronisations) and raises KDError on a device error.
@@ -380,7 +411,12 @@ def topk_kl_loss(h, W, teacher_idx, teacher_logits, valid, tau, chunk=4096):
     for t, _, name in args:
         if not t.is_cuda:
             raise ValueError(f"{name} must be a CUDA tensor")
-    return _TopKKLFunction.apply(h, W, teacher_idx, teacher_logits, valid, tau, chunk)
+        if t.device != h.device:
+            raise ValueError(f"{name} is on {t.device} but h is on {h.device}: all inputs must "
+                             f"be on one CUDA device")
+    # the library launches on the current device: make it the inputs' device
+    with torch.cuda.device(h.device):
+        return _TopKKLFunction.apply(h, W, teacher_idx, teacher_logits, valid, tau, chunk)
 
 
 class TopKKL:

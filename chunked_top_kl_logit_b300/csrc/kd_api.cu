@@ -267,7 +267,8 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c
   static bool attr_ok[64];
   if (!ensure_smem_attr(kd_gemm_kernel<MODE>, attr_once, attr_ok)) return KD_ERR_CUDA;
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-  const int slot = MODE == EPI_STORE ? -1 : timing_slot(MODE);
+  // the residual variant's forward is timed as the forward logit kernel
+  const int slot = MODE == EPI_STORE ? -1 : timing_slot(MODE == EPI_FWD_RESID ? EPI_FWD : MODE);
   if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
     return KD_ERR_CUDA;
   kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, c, dm, p);
@@ -338,12 +339,12 @@ Ws carve(void* ws, const Layout& L) {
 // Normalisation of the teacher's cached entries.  Main loss: all pointers null
 // (softmax renormalised over the K entries).  Residual variant: teacher_lse is
 // the teacher's full-vocabulary log-normaliser at tau; the forward writes the
-// student's mass on the cached entries to topk_mass_out and the backward reads
-// it back from topk_mass_in.
+// student's mass outside the cached entries to outside_mass_out and the
+// backward reads it back from outside_mass_in.
 struct Variant {
   const float* teacher_lse = nullptr;
-  float* topk_mass_out = nullptr;
-  const float* topk_mass_in = nullptr;
+  float* outside_mass_out = nullptr;
+  const float* outside_mass_in = nullptr;
   bool residual() const { return teacher_lse != nullptr; }
 };
 
@@ -456,6 +457,7 @@ const char* kd_topk_kl_status_string(int status) {
     case KD_ERR_TIMEOUT: return "bounded pipeline wait timed out";
     case KD_ERR_SCRATCH_LIMIT: return "shape needs more than the built-in 32 MiB scratch array";
     case KD_ERR_INTERNAL: return "internal bound violated (library bug)";
+    case KD_ERR_NONFINITE: return "a row of teacher logits is not finite (NaN or +inf)";
     default: return "unknown status";
   }
 }
@@ -515,12 +517,14 @@ int enqueue_forward(const void* h, const void* W, const uint8_t* valid, int64_t 
   p.part = part;
   p.zg = zg;
   p.gidx = gathered_idx;
-  if ((rc = launch_gemm<EPI_FWD>(ta, tb, ta, ta, p, sms, st))) return rc;
+  rc = var.residual() ? launch_gemm<EPI_FWD_RESID>(ta, tb, ta, ta, p, sms, st)
+                      : launch_gemm<EPI_FWD>(ta, tb, ta, ta, p, sms, st);
+  if (rc) return rc;
 
   const int nb = static_cast<int>(cdiv(T, 32));
   kd_combine_kernel<<<nb, dim3(32, COMBINE_SPLIT), 0, st>>>(
-      part, p.n_tiles, static_cast<int>(T), K, w.sp, zg, w.tterm,
-      var.residual() ? w.resid : nullptr, valid, lse, row_kl, var.topk_mass_out, w.losspart);
+      part, p.n_tiles, static_cast<int>(T), K, w.sidx, w.sp, zg, w.tterm,
+      var.residual() ? w.resid : nullptr, valid, lse, row_kl, var.outside_mass_out, w.losspart);
   kd_loss_final_kernel<<<1, 256, 0, st>>>(w.losspart, nb, w.nvalid, loss);
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
@@ -582,7 +586,7 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
     p.c_log2 = LOG2E * inv_tau;
     p.lse = lse;
     p.resid = var.residual() ? w.resid : nullptr;
-    p.topk_mass = var.topk_mass_in;
+    p.outside_mass = var.outside_mass_in;
     p.valid = valid;
     p.nvalid = w.nvalid;
     p.grad_loss = grad_loss;
@@ -915,7 +919,8 @@ int kd_topk_kl_forward_residual(const void* h, const void* W, const int32_t* tea
                                 const float* teacher_logits, const float* teacher_lse,
                                 const uint8_t* valid, int64_t T, int64_t V, int64_t d, int32_t K,
                                 float tau, int64_t chunk, float* loss, float* lse, float* row_kl,
-                                float* topk_mass, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                float* outside_mass, void* ws, size_t ws_bytes,
+                                int32_t* dev_status,
                                 struct CUstream_st* stream) {
   int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
                         dev_status);
@@ -931,7 +936,7 @@ int kd_topk_kl_forward_residual(const void* h, const void* W, const int32_t* tea
   const Ws w = carve(ws, L);
   Variant var;
   var.teacher_lse = teacher_lse;
-  var.topk_mass_out = topk_mass;
+  var.outside_mass_out = outside_mass;
   if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
                      st)))
     return rc;
@@ -943,15 +948,15 @@ int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* te
                                  const float* teacher_logits, const float* teacher_lse,
                                  const uint8_t* valid, int64_t T, int64_t V, int64_t d, int32_t K,
                                  float tau, int64_t chunk, const float* lse,
-                                 const float* topk_mass, float grad_loss, float* dh, float* dW,
+                                 const float* outside_mass, float grad_loss, float* dh, float* dW,
                                  void* ws, size_t ws_bytes, int32_t* dev_status,
                                  struct CUstream_st* stream) {
   int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
                         dev_status);
   if (rc != KD_OK) return rc;
-  if (!lse || !topk_mass || !teacher_lse || !dh || !dW || !aligned16(dh) || !aligned16(dW) ||
+  if (!lse || !outside_mass || !teacher_lse || !dh || !dW || !aligned16(dh) || !aligned16(dW) ||
       (reinterpret_cast<uintptr_t>(teacher_lse) & 3u) ||
-      (reinterpret_cast<uintptr_t>(topk_mass) & 3u))
+      (reinterpret_cast<uintptr_t>(outside_mass) & 3u))
     return KD_ERR_INVALID_ARG;
   if (!std::isfinite(grad_loss)) return KD_ERR_INVALID_ARG;
   const Layout L = make_layout(T, V, d, K, chunk);
@@ -963,7 +968,7 @@ int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* te
   const Ws w = carve(ws, L);
   Variant var;
   var.teacher_lse = teacher_lse;
-  var.topk_mass_in = topk_mass;
+  var.outside_mass_in = outside_mass;
   if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
                      st)))
     return rc;
@@ -1029,7 +1034,7 @@ int kd_teacher_topk(const void* h, const void* W, int64_t T, int64_t V, int64_t 
     const unsigned blocks = static_cast<unsigned>(cdiv(rows, TOPK_WARPS));
     kd_topk_threshold_kernel<<<blocks, 32 * TOPK_WARPS, 0, st>>>(
         tkeys, part, rows, static_cast<int>(rows), L.n_tiles, K, theta, theta_val,
-        full_lse ? full_lse + c0 : nullptr);
+        full_lse ? full_lse + c0 : nullptr, dev_status);
     if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(rows) * 4, st) != cudaSuccess)
       return KD_ERR_CUDA;
     // candidates at or above the threshold, from the stored logits
@@ -1043,7 +1048,8 @@ int kd_teacher_topk(const void* h, const void* W, int64_t T, int64_t V, int64_t 
         cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
       return KD_ERR_CUDA;
     kd_topk_finalize_kernel<<<blocks, 32 * TOPK_WARPS, 0, st>>>(
-        cand, cnt, L.cap, static_cast<int>(rows), K, topk_idx + c0 * K, topk_logits + c0 * K);
+        cand, cnt, L.cap, theta_val, static_cast<int>(rows), K, topk_idx + c0 * K,
+        topk_logits + c0 * K, dev_status);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
   }
   return KD_OK;

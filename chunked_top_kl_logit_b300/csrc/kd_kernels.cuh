@@ -47,13 +47,16 @@ constexpr float LN2 = 0.6931471805599453f;
 // accumulated; they differ only in schedule, and are separate instantiations
 // so that profiles tell them apart.
 // EPI_TMAX: the contraction of the teacher-side top-K producer.
+// EPI_FWD_RESID: the forward of the residual-mass variant, whose lse partials
+// cover only the columns outside the row's cache.
 enum EpiMode {
   EPI_FWD = 0,
   EPI_DZ = 1,
   EPI_STORE = 2,
   EPI_DH = 3,
   EPI_DW = 4,
-  EPI_TMAX = 5
+  EPI_TMAX = 5,
+  EPI_FWD_RESID = 6
 };
 
 struct GemmParams {
@@ -93,7 +96,7 @@ struct GemmParams {
   int* gidx;              // [T][K] (slot order) vocabulary column read, or null
   const float* lse;       // [T]
   const float* resid;     // [T] teacher mass outside the cached entries, or null (main loss)
-  const float* topk_mass; // [T] student mass on the cached entries (with resid)
+  const float* outside_mass; // [T] student mass outside the cached entries (with resid)
   const uint8_t* valid;   // [T]
   const int* nvalid;      // device scalar
   float grad_loss;
@@ -309,8 +312,37 @@ __device__ __forceinline__ void mma_role(const GemmParams& p, const Sched& sc, u
 
 // ------------------------------------------------------------------ epilogues
 
+// Gather z/tau at the row's cached entries that fall in the 32 columns from
+// cb (the sorted walk: pos / nxt are the row's next entry and its column) and
+// return the mask of those columns.  Warp-uniform loop, one entry per lane
+// per iteration, the register picked by a 32-way select.
+__device__ __forceinline__ uint32_t gather_chunk(const GemmParams& p, const uint32_t (&r)[32],
+                                                 int cb, int64_t grow, const int* srow, int& pos,
+                                                 int& nxt) {
+  uint32_t hit = 0u;
+  const int ce = cb + 32;
+  while (__any_sync(0xffffffffu, nxt < ce)) {
+    if (nxt < ce) {
+      const int j = nxt - cb;
+      uint32_t bits = 0;
+#pragma unroll
+      for (int jj = 0; jj < 32; ++jj) bits = (jj == j) ? r[jj] : bits;
+      p.zg[grow * p.K + pos] = __uint_as_float(bits) * p.inv_tau;
+      if (p.gidx) p.gidx[grow * p.K + p.sslot[grow * p.K + pos]] = nxt;
+      hit |= 1u << j;
+      ++pos;
+      nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
+    }
+  }
+  return hit;
+}
+
 // Forward: per (row, vocab tile) natural-log lse partial of z/tau and the
 // gather of z/tau at the row's cached indices that fall inside the tile.
+// EXCL (residual-mass variant): the partial leaves out the cached columns, so
+// that the mass outside the cache is a sum of its own terms, never 1 minus
+// the cached mass.
+template <bool EXCL>
 __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, const TileCoord& c,
                                         int acc,
                                         uint32_t tmem_row, int r_in_tile, uint64_t* tfull,
@@ -340,6 +372,26 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
     uint32_t r[32];
     tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
     tmem_ld_wait(r);
+    if (EXCL) {  // gather first, then sum the columns the gather did not hit
+      const uint32_t hit = gather_chunk(p, r, cb, grow, srow, pos, nxt);
+      float u[32];
+      float cm = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        u[j] = (cb + j < p.N && !((hit >> j) & 1u)) ? __uint_as_float(r[j]) * p.c_log2
+                                                     : -CUDART_INF_F;
+        cm = fmaxf(cm, u[j]);
+      }
+      const float mn = fmaxf(m, cm);
+      if (mn != -CUDART_INF_F) {  // else nothing outside the cache so far
+        float cs = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) cs += ex2f(u[j] - mn);
+        s = s * ex2f(m - mn) + cs;
+        m = mn;
+      }
+      continue;
+    }
     float cs = 0.f;
     if (cb + 32 <= p.N) {  // uniform: all 32 columns inside the vocabulary
       // max on the raw logits (c > 0), then one FFMA + one ex2 per element
@@ -365,19 +417,7 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
       s = s * ex2f(m - mn) + cs;
       m = mn;
     }
-    const int ce = cb + 32;
-    while (__any_sync(0xffffffffu, nxt < ce)) {
-      if (nxt < ce) {
-        const int j = nxt - cb;
-        uint32_t bits = 0;
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) bits = (jj == j) ? r[jj] : bits;
-        p.zg[grow * p.K + pos] = __uint_as_float(bits) * p.inv_tau;
-        if (p.gidx) p.gidx[grow * p.K + p.sslot[grow * p.K + pos]] = nxt;
-        ++pos;
-        nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
-      }
-    }
+    gather_chunk(p, r, cb, grow, srow, pos, nxt);
   }
   tc_fence_before();
   mbar_arrive(&tempty[acc]);
@@ -409,7 +449,7 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
       lb = p.lse[grow] * LOG2E;
       if (p.resid) {
         const float R = p.resid[grow];
-        if (R > 0.f) rq = R / (1.f - p.topk_mass[grow]);
+        if (R > 0.f) rq = R / p.outside_mass[grow];
       }
       pos = lower_bound_row(srow, p.K, v0);
       nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
@@ -831,8 +871,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (MODE == EPI_DW)
         epi_dw(p, sc, c, acc, tmem_row, q, tfull, tempty, use, abort_flag, ok, &tmC, &tmD,
                my_stage, piece);
-      else if (MODE == EPI_FWD)
-        epi_fwd(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok);
+      else if (MODE == EPI_FWD || MODE == EPI_FWD_RESID)
+        epi_fwd<MODE == EPI_FWD_RESID>(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use,
+                                       abort_flag, ok);
       else if (MODE == EPI_DZ)
         epi_dz(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok, &tmC,
                my_stage, piece);
@@ -943,65 +984,95 @@ __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restr
 // cached entry) from y, so a warp reads 32 consecutive rows of one tile's
 // partials (coalesced); the COMBINE_SPLIT partial results of a row are merged
 // in the fixed order y = 0, 1, ...
-// resid != null (residual variant): the student mass on the cached entries,
-// s = sum_k exp(zg_k - lse), goes to topk_mass_out (if given) and row_kl gains
-// R (log R - log(1 - s)) for R > 0.
+// resid != null (residual variant): the partials cover only the columns
+// outside the row's cache (lse_out = Lu over those); the cached columns, each
+// distinct index once (sidx is ascending), complete the normaliser, lse =
+// log(exp(Lu) + sum exp(zg)).  The student mass outside the cache is then
+// Q = exp(Lu - lse), less the mass of repeated slots (each slot is its own
+// outcome), with no 1 - sum cancellation; it goes to outside_mass_out (if
+// given) and row_kl gains R (log R - log Q) for R > 0.
 constexpr int COMBINE_SPLIT = 8;
+
+__device__ __forceinline__ void online_lse_add(float v, float& m, float& s) {
+  if (v == -CUDART_INF_F) return;  // exp(-inf) adds nothing
+  if (v > m) {
+    s = s * expf(m - v) + 1.f;
+    m = v;
+  } else {
+    s += expf(v - m);
+  }
+}
+
+// Fixed-order merge of the COMBINE_SPLIT (max, sum) pairs of column x.
+__device__ __forceinline__ float merge_lse(const float (&sm)[COMBINE_SPLIT][32],
+                                           const float (&ss)[COMBINE_SPLIT][32], int x) {
+  float M = sm[0][x], S = ss[0][x];
+  for (int i = 1; i < COMBINE_SPLIT; ++i) {
+    const float mi = sm[i][x], si = ss[i][x];
+    const float mn = fmaxf(M, mi);
+    if (mn != -CUDART_INF_F) S = S * expf(M - mn) + si * expf(mi - mn);
+    M = mn;
+  }
+  return M + logf(S);
+}
 
 __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
     kd_combine_kernel(const float* __restrict__ part, int n_tiles, int T, int K,
-                      const float* __restrict__ sp, const float* __restrict__ zg,
-                      const float* __restrict__ tterm, const float* __restrict__ resid,
-                      const uint8_t* __restrict__ valid, float* __restrict__ lse_out,
-                      float* __restrict__ row_kl_out, float* __restrict__ topk_mass_out,
-                      double* __restrict__ losspart) {
+                      const int* __restrict__ sidx, const float* __restrict__ sp,
+                      const float* __restrict__ zg, const float* __restrict__ tterm,
+                      const float* __restrict__ resid, const uint8_t* __restrict__ valid,
+                      float* __restrict__ lse_out, float* __restrict__ row_kl_out,
+                      float* __restrict__ outside_mass_out, double* __restrict__ losspart) {
   __shared__ float sm[COMBINE_SPLIT][32], ss[COMBINE_SPLIT][32];
-  __shared__ float s_lse[32];
+  __shared__ float s_lse[32], s_lu[32];
   __shared__ float sa[COMBINE_SPLIT][32], smass[COMBINE_SPLIT][32];
   __shared__ double red[32];
   const int x = threadIdx.x, y = threadIdx.y;
   const int row = blockIdx.x * 32 + x;
   const bool in = row < T;
+  const int64_t rk0 = static_cast<int64_t>(row) * K;
   // online logsumexp over this thread's tiles
   float m = -CUDART_INF_F;
   float s = 0.f;
-  if (in) {
-    for (int j = y; j < n_tiles; j += COMBINE_SPLIT) {
-      const float v = part[static_cast<int64_t>(j) * T + row];
-      if (v > m) {
-        s = s * expf(m - v) + 1.f;
-        m = v;
-      } else {
-        s += expf(v - m);
-      }
-    }
-  }
+  if (in)
+    for (int j = y; j < n_tiles; j += COMBINE_SPLIT)
+      online_lse_add(part[static_cast<int64_t>(j) * T + row], m, s);
   sm[y][x] = m;
   ss[y][x] = s;
   __syncthreads();
   if (y == 0) {
-    float M = sm[0][x], S = ss[0][x];
-    for (int i = 1; i < COMBINE_SPLIT; ++i) {
-      const float mi = sm[i][x], si = ss[i][x];
-      const float mn = fmaxf(M, mi);
-      if (mn != -CUDART_INF_F) S = S * expf(M - mn) + si * expf(mi - mn);
-      M = mn;
-    }
-    const float lse = M + logf(S);
-    s_lse[x] = lse;
-    if (in && lse_out) lse_out[row] = lse;
+    const float L = merge_lse(sm, ss, x);
+    s_lse[x] = L;
+    if (in && lse_out && !resid) lse_out[row] = L;
   }
   __syncthreads();
+  if (resid) {  // uniform: the cached columns complete the normaliser
+    m = -CUDART_INF_F;
+    s = 0.f;
+    if (in)
+      for (int k = y; k < K; k += COMBINE_SPLIT)
+        if (k == 0 || sidx[rk0 + k] != sidx[rk0 + k - 1]) online_lse_add(zg[rk0 + k], m, s);
+    sm[y][x] = m;
+    ss[y][x] = s;
+    __syncthreads();
+    if (y == 0) {
+      const float Lu = s_lse[x];
+      const float Lc = merge_lse(sm, ss, x);
+      const float L = fmaxf(Lu, Lc) + log1pf(expf(-fabsf(Lu - Lc)));  // Lc is finite
+      s_lu[x] = Lu;
+      s_lse[x] = L;
+      if (in && lse_out) lse_out[row] = L;
+    }
+    __syncthreads();
+  }
   const float lse = s_lse[x];
-  // this thread's share of sum_k p_k (lse - zg_k) and of sum_k exp(zg_k - lse)
+  // this thread's share of sum_k p_k (lse - zg_k) and of the repeated slots' mass
   float acc = 0.f, mass = 0.f;
   if (in) {
-    const float* pr = sp + static_cast<int64_t>(row) * K;
-    const float* zr = zg + static_cast<int64_t>(row) * K;
     for (int k = y; k < K; k += COMBINE_SPLIT) {
-      const float zk = zr[k];
-      acc += pr[k] * (lse - zk);
-      if (resid) mass += expf(zk - lse);
+      const float zk = zg[rk0 + k];
+      acc += sp[rk0 + k] * (lse - zk);
+      if (resid && k > 0 && sidx[rk0 + k] == sidx[rk0 + k - 1]) mass += expf(zk - lse);
     }
   }
   sa[y][x] = acc;
@@ -1010,18 +1081,24 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
   if (y == 0) {
     double kl = 0.0;
     if (in) {
-      float a = 0.f, ms = 0.f;
+      float a = 0.f, dup = 0.f;
       for (int i = 0; i < COMBINE_SPLIT; ++i) {
         a += sa[i][x];
-        ms += smass[i][x];
+        dup += smass[i][x];
       }
-      if (resid && topk_mass_out) topk_mass_out[row] = ms;
+      float Q = 0.f, logQ = 0.f;
+      if (resid) {
+        const float lu = s_lu[x] - lse;
+        Q = expf(lu) - dup;
+        logQ = dup == 0.f ? lu : logf(Q);
+        if (outside_mass_out) outside_mass_out[row] = Q;
+      }
       float rk = 0.f;
       if (valid[row]) {
         rk = tterm[row] + a;
         if (resid) {
           const float R = resid[row];
-          if (R > 0.f) rk += R * (logf(R) - log1pf(-ms));
+          if (R > 0.f) rk += R * (logf(R) - logQ);
         }
       }
       if (row_kl_out) row_kl_out[row] = rk;

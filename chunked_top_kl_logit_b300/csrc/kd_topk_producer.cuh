@@ -78,13 +78,16 @@ constexpr int TOPK_WARPS = 8;  // rows per block of the SIMT kernels
 
 // One warp per row of the chunk: the threshold key (theta = 0, i.e. every
 // logit a candidate, when the row has fewer than K tiles), its logit value,
-// and the row's full-vocabulary lse of z / tau from the tile partials.
+// and the row's full-vocabulary lse of z / tau from the tile partials.  A NaN
+// or +inf logit makes its tile's partial NaN (and a tile of -inf logits gives
+// one too), so a row whose lse is not finite is flagged: theta_val = NaN,
+// which no logit passes in the scan, and KD_ERR_NONFINITE.
 __global__ void kd_topk_threshold_kernel(const uint64_t* __restrict__ tkeys,
                                          const float* __restrict__ part, int64_t part_ld,
                                          int rows, int n_tiles, int K,
                                          uint64_t* __restrict__ theta,
                                          float* __restrict__ theta_val,
-                                         float* __restrict__ full_lse) {
+                                         float* __restrict__ full_lse, int* status) {
   __shared__ uint32_t hist[TOPK_WARPS][256];
   const int wid = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -113,9 +116,14 @@ __global__ void kd_topk_threshold_kernel(const uint64_t* __restrict__ tkeys,
     m = mn;
   }
   if (lane == 0) {
+    const float lse = m + logf(s);
+    const bool finite = isfinite(lse);
     theta[row] = th;
-    theta_val[row] = th ? float_from_order_key(static_cast<uint32_t>(th >> 32)) : -CUDART_INF_F;
-    if (full_lse) full_lse[row] = m + logf(s);
+    theta_val[row] = !finite ? CUDART_NAN_F
+                   : th     ? float_from_order_key(static_cast<uint32_t>(th >> 32))
+                            : -CUDART_INF_F;
+    if (full_lse) full_lse[row] = finite ? lse : CUDART_NAN_F;
+    if (!finite) set_status(status, KD_ERR_NONFINITE);
   }
 }
 
@@ -166,11 +174,16 @@ __global__ void __launch_bounds__(SCAN_THREADS)
   }
 }
 
-// One warp per row: the K largest candidate keys, in descending order.
+// One warp per row: the K largest candidate keys, in descending order.  A row
+// flagged non-finite (theta_val NaN), or one with fewer than K candidates
+// (which the threshold bound rules out for finite rows: KD_ERR_INTERNAL), is
+// written as index -1 and value NaN; no candidate slot past the row's count
+// is ever read.
 __global__ void kd_topk_finalize_kernel(uint64_t* __restrict__ cand,
-                                        const int* __restrict__ cand_cnt, int cand_cap, int rows,
-                                        int K, int32_t* __restrict__ out_idx,
-                                        float* __restrict__ out_val) {
+                                        const int* __restrict__ cand_cnt, int cand_cap,
+                                        const float* __restrict__ theta_val, int rows, int K,
+                                        int32_t* __restrict__ out_idx,
+                                        float* __restrict__ out_val, int* status) {
   __shared__ uint32_t hist[TOPK_WARPS][256];
   const int wid = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -178,6 +191,17 @@ __global__ void kd_topk_finalize_kernel(uint64_t* __restrict__ cand,
   if (row >= rows) return;
   uint64_t* c = cand + static_cast<int64_t>(row) * cand_cap;
   const int n = min(cand_cnt[row], cand_cap);
+  int32_t* oi = out_idx + static_cast<int64_t>(row) * K;
+  float* ov = out_val + static_cast<int64_t>(row) * K;
+  const bool flagged = isnan(theta_val[row]);
+  if (flagged || n < K) {  // warp-uniform
+    if (!flagged && lane == 0) set_status(status, KD_ERR_INTERNAL);
+    for (int i = lane; i < K; i += 32) {
+      oi[i] = -1;
+      ov[i] = CUDART_NAN_F;
+    }
+    return;
+  }
   const uint64_t kth = warp_kth_largest(c, n, K, hist[wid]);
   // move the K keys >= kth to the front (reads of a 32-key block precede its
   // writes, and writes never pass the block being read)
@@ -193,8 +217,6 @@ __global__ void kd_topk_finalize_kernel(uint64_t* __restrict__ cand,
     __syncwarp();
   }
   // rank by pairwise comparison among the K and write in descending order
-  int32_t* oi = out_idx + static_cast<int64_t>(row) * K;
-  float* ov = out_val + static_cast<int64_t>(row) * K;
   for (int i = lane; i < K; i += 32) {
     const uint64_t key = c[i];
     int r = 0;

@@ -73,7 +73,8 @@ typedef enum kd_status {
   KD_ERR_INDEX_RANGE = 5,  /* device: a teacher index is outside [0, V) */
   KD_ERR_TIMEOUT = 6,      /* device: a bounded pipeline wait ran out */
   KD_ERR_SCRATCH_LIMIT = 7, /* kd_topk_kl_forward_noalloc: shape too big for its scratch */
-  KD_ERR_INTERNAL = 8       /* device: an internal bound proved false (a library bug) */
+  KD_ERR_INTERNAL = 8,      /* device: an internal bound proved false (a library bug) */
+  KD_ERR_NONFINITE = 9      /* device (kd_teacher_topk): a row's logits are not all finite */
 } kd_status;
 
 /*
@@ -180,23 +181,28 @@ int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* tea
  *   G_tv = s_t / tau (q_tv (1 - R_t/Q_t) + (R_t/Q_t) c_tv q_tv - sum_{k: idx_tk = v} P_tk)
  *   with s_t = grad_loss valid_t / N_valid and c_tv the number of slots holding v.
  *
- * The forward also writes topk_mass_t = sum_k q_tk (fp32 [T], device, or
- * NULL); the backward needs it (with lse) from the forward.  Other arguments,
- * outputs, workspace sizes and errors as kd_topk_kl_forward / _backward.  A row
- * whose student puts all its mass on the cached entries (Q_t = 0) while
- * R_t > 0 has an infinite loss, as the definition says.
+ * The forward also writes outside_mass_t = Q_t (fp32 [T], device, or NULL);
+ * the backward needs it (with lse) from the forward.  Q_t is not formed as
+ * 1 - sum_k q_tk, which loses every digit in fp32 once the student puts
+ * nearly all its mass on the cached entries (the well-distilled regime): the
+ * forward sums the columns outside the cache on their own (their log-sum-exp
+ * Lu_t), so Q_t = exp(Lu_t - lse_t) to fp32 relative precision (a row that
+ * repeats an index subtracts that slot's extra q).  Other arguments, outputs,
+ * workspace sizes and errors as kd_topk_kl_forward / _backward.  A row whose
+ * student puts all its mass on the cached entries (Q_t = 0) while R_t > 0 has
+ * an infinite loss, as the definition says.
  */
 int kd_topk_kl_forward_residual(const void* h, const void* W, const int32_t* teacher_idx,
                                 const float* teacher_logits, const float* teacher_lse,
                                 const uint8_t* valid, int64_t T, int64_t V, int64_t d, int32_t K,
                                 float tau, int64_t chunk, float* loss, float* lse, float* row_kl,
-                                float* topk_mass, void* ws, size_t ws_bytes, int32_t* dev_status,
-                                struct CUstream_st* stream);
+                                float* outside_mass, void* ws, size_t ws_bytes,
+                                int32_t* dev_status, struct CUstream_st* stream);
 int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* teacher_idx,
                                  const float* teacher_logits, const float* teacher_lse,
                                  const uint8_t* valid, int64_t T, int64_t V, int64_t d, int32_t K,
                                  float tau, int64_t chunk, const float* lse,
-                                 const float* topk_mass, float grad_loss, float* dh, float* dW,
+                                 const float* outside_mass, float grad_loss, float* dh, float* dW,
                                  void* ws, size_t ws_bytes, int32_t* dev_status,
                                  struct CUstream_st* stream);
 
@@ -221,9 +227,13 @@ int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* te
  * The workspace holds one chunk's logits and candidates:
  * kd_teacher_topk_workspace_size(...) ~ chunk * (4 V + 8 min(V, (K - 1) * 256 + 1))
  * bytes (3.3 GB + 0.8 GB at chunk = 4096, V = 201088, K = 100); a smaller chunk
- * bounds it.  Inputs must be finite.  Limits and errors as kd_topk_kl_forward
- * (KD_ERR_INTERNAL in *dev_status would mean a candidate bound was exceeded,
- * which the construction rules out).  Deterministic.
+ * bounds it.  Limits and errors as kd_topk_kl_forward (KD_ERR_INTERNAL in
+ * *dev_status would mean a candidate bound was exceeded, which the
+ * construction rules out).  A row whose logits include NaN or +inf (from
+ * non-finite or overflowing h or W), or whose full-vocabulary normaliser is
+ * not finite, has no defined top-K: the call sets KD_ERR_NONFINITE and writes
+ * that row as topk_idx = -1, topk_logits = NaN, full_lse = NaN; the other rows
+ * are unaffected.  Deterministic.
  */
 int kd_teacher_topk_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk,
                                    size_t* bytes);

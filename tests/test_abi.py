@@ -34,7 +34,7 @@ def test_header_symbols_exported():
 
 
 def test_status_strings():
-    for code in range(9):
+    for code in range(10):
         s = kd.status_string(code)
         assert isinstance(s, str) and s and s != "unknown status"
     assert kd.status_string(99) == "unknown status"
@@ -157,7 +157,7 @@ def test_forward_backward_argument_checks():
 
 
 def test_residual_entry_argument_checks():
-    """The residual-mass entries need teacher_lse (and the backward topk_mass)
+    """The residual-mass entries need teacher_lse (and the backward outside_mass)
     and reject their absence before any CUDA call."""
     vp = ctypes.c_void_p
     L = kd.lib()
@@ -226,3 +226,56 @@ def test_autograd_adapter_checks_inputs_before_any_call():
         kd.topk_kl_loss(h, W, idx.long(), tl, valid, 1.0, 4)
     with pytest.raises(ValueError):
         kd.topk_kl_loss(h, W, idx, tl, valid, 1.0, 4)  # host tensors
+
+
+class _FakeCuda:
+    """Stands in for a CUDA tensor on device `index` (shape, dtype and device
+    only); the checks below must reject it before anything reaches the library."""
+
+    def __init__(self, shape, dtype, index):
+        import torch
+        self.shape, self.dtype, self.is_cuda = shape, dtype, True
+        self.device = torch.device("cuda", index)
+
+
+def test_autograd_adapter_rejects_inputs_on_two_devices():
+    import torch
+    T, V, d, K = 4, 1024, 64, 2
+    args = [_FakeCuda((T, d), torch.bfloat16, 0), _FakeCuda((V, d), torch.bfloat16, 0),
+            _FakeCuda((T, K), torch.int32, 0), _FakeCuda((T, K), torch.float32, 0),
+            _FakeCuda((T,), torch.uint8, 0)]
+    for i in range(1, 5):
+        a = list(args)
+        a[i] = _FakeCuda(a[i].shape, a[i].dtype, 1)
+        with pytest.raises(ValueError, match="one CUDA device"):
+            kd.topk_kl_loss(*a, 1.0, 4)
+
+
+def test_wrappers_reject_tensors_off_the_current_device(monkeypatch):
+    """Every wrapper checks that its tensors and stream are on the current
+    device (the library launches there) before calling into the library."""
+    import torch
+
+    class _Stream:
+        device = torch.device("cuda", 0)
+        cuda_stream = 0
+
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 0)
+    monkeypatch.setattr(torch.cuda, "current_stream", lambda device=None: _Stream())
+    T, V, d, K = 4, 1024, 64, 2
+    on0 = dict(h=_FakeCuda((T, d), torch.bfloat16, 0), W=_FakeCuda((V, d), torch.bfloat16, 0),
+               teacher_idx=_FakeCuda((T, K), torch.int32, 0),
+               teacher_logits=_FakeCuda((T, K), torch.float32, 0),
+               valid=_FakeCuda((T,), torch.uint8, 0))
+    out = dict(loss=_FakeCuda((1,), torch.float32, 0), lse=_FakeCuda((T,), torch.float32, 0))
+    for name in list(on0) + ["loss", "ws"]:
+        kw = dict(on0, **out)
+        ws = _FakeCuda((64,), torch.uint8, 0)
+        if name == "ws":
+            ws = _FakeCuda((64,), torch.uint8, 1)
+        else:
+            kw[name] = _FakeCuda(kw[name].shape, kw[name].dtype, 1)
+        with pytest.raises(ValueError, match="current device"):
+            kd.kd_topk_kl_forward(kw["h"], kw["W"], kw["teacher_idx"], kw["teacher_logits"],
+                                  kw["valid"], 1.0, 4, kw["loss"], kw["lse"], ws=ws,
+                                  dev_status=_FakeCuda((1,), torch.int32, 0))

@@ -155,3 +155,62 @@ def test_producer_k_larger_than_tile_count():
     h = torch.randn(T, d, generator=g).to(torch.bfloat16)
     W = (torch.randn(V, d, generator=g) / math.sqrt(d)).to(torch.bfloat16)
     check_against_oracle(h, W, K, 1.0, 64)
+
+
+KD_ERR_NONFINITE = 9
+
+
+def test_producer_nonfinite_rows_are_reported():
+    """Rows of h holding NaN or inf (host-made inputs, so their logits hold
+    NaN and +-inf): the call reports KD_ERR_NONFINITE, writes those rows as
+    index -1, logit NaN and lse NaN, and every other row is still the oracle's
+    result bit for bit (integer inputs).  The bad rows sit in both chunks."""
+    g = torch.Generator().manual_seed(19)
+    T, V, d, K, chunk = 96, 3000, 64, 20, 64
+    h = torch.randint(-2, 3, (T, d), generator=g).to(torch.bfloat16)
+    W = torch.randint(-1, 2, (V, d), generator=g).to(torch.bfloat16)
+    h[3, 5] = float("nan")
+    h[40, :] = float("inf")
+    h[95, 0] = float("-inf")
+    bad = np.array([3, 40, 95])
+    dev = torch.device("cuda")
+    ws = torch.empty(kd.kd_teacher_topk_workspace_size(T, V, d, K, chunk), dtype=torch.uint8,
+                     device=dev)
+    # stale candidates from a clean run must not leak into the flagged rows
+    clean = h.clone()
+    clean[bad] = 1.0
+    st = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    idx = torch.full((T, K), -7, dtype=torch.int32, device=dev)
+    val = torch.zeros((T, K), dtype=torch.float32, device=dev)
+    lse = torch.zeros(T, dtype=torch.float32, device=dev)
+    kd.kd_teacher_topk(clean.to(dev), W.to(dev), K, 1.0, chunk, idx, val, lse, ws=ws,
+                       dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    kd.kd_teacher_topk(h.to(dev), W.to(dev), K, 1.0, chunk, idx, val, lse, ws=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == KD_ERR_NONFINITE, kd.status_string(int(st.item()))
+    gi, gv, gl = idx.cpu().numpy(), val.cpu().numpy(), lse.cpu().numpy()
+    assert np.all(gi[bad] == -1) and np.all(np.isnan(gv[bad])) and np.all(np.isnan(gl[bad]))
+    good = np.setdiff1d(np.arange(T), bad)
+    oi, ov, ol = TK.teacher_topk(h[good].double().numpy(), W.double().numpy(), K, 1.0)
+    np.testing.assert_array_equal(gi[good], oi)
+    np.testing.assert_array_equal(gv[good], ov)
+    assert np.abs(gl[good] - ol).max() <= LSE_ATOL
+
+
+def test_producer_signed_zero_logits():
+    """Integer inputs whose top logits are exact zeros of either sign (h >= 0,
+    W in {-1, 0}, mostly 0): -0 and +0 are one value, so the top-K are the
+    lowest indices among the zero logits, exactly as the oracle orders them."""
+    g = torch.Generator().manual_seed(23)
+    T, V, d, K = 128, 4096, 64, 100
+    h = torch.randint(0, 3, (T, d), generator=g).to(torch.bfloat16)
+    W = -(torch.rand(V, d, generator=g) < 0.02).to(torch.bfloat16)
+    gi, gv, gl = run_producer(h, W, K, 1.0, 64)
+    oi, ov, ol = TK.teacher_topk(h.double().numpy(), W.double().numpy(), K, 1.0)
+    z = h.double().numpy() @ W.double().numpy().T
+    assert np.all((z == 0).sum(axis=1) >= K)  # the top-K of every row are zeros
+    np.testing.assert_array_equal(gi, oi)
+    np.testing.assert_array_equal(gv, ov)
+    assert np.abs(gl - ol).max() <= LSE_ATOL

@@ -89,3 +89,18 @@ def test_top_k_in_one_tile_and_ascending_rows():
 def test_fewer_tiles_than_k_takes_the_whole_row():
     z = np.random.default_rng(3).standard_normal(700).astype(np.float32)
     assert candidates(z, 16).shape[0] == 700
+
+
+def test_signed_zeros_count_as_one_value():
+    """-0.0 and +0.0 are one logit value (the producer folds -0 into +0 before
+    forming keys, and numpy's ordering treats them as equal): mixed signed
+    zeros at the top of a row order by index alone, and the bound holds."""
+    rng = np.random.default_rng(5)
+    for V, K in [(64 * TILE, 8), (201088 // 8, 100)]:
+        z = np.where(rng.random(V) < 0.5, np.float32(-0.0), np.float32(0.0))
+        z[rng.random(V) < 0.3] = -1.0
+        assert np.signbit(z[z == 0]).any() and (~np.signbit(z[z == 0])).any()
+        cand = check(z, K)
+        top = np.nonzero(key_ranks(z) < K)[0]
+        np.testing.assert_array_equal(top, np.nonzero(z == 0)[0][:K])
+        assert cand.shape[0] <= (K - 1) * TILE + 1
