@@ -28,17 +28,20 @@ import torch
 __all__ = [
     "KD_OK", "KDError", "lib", "library_path", "status_string",
     "kd_topk_kl_workspace_size", "kd_topk_kl_launch_count", "kd_topk_kl_forward",
+    "kd_topk_kl_forward_backward_workspace_size",
     "kd_topk_kl_forward_noalloc", "kd_topk_kl_backward", "kd_topk_kl_forward_backward",
     "KD_ACCUMULATE_DW", "kd_entropy_filter_workspace_size", "kd_entropy_filter",
     "kd_topk_kl_forward_residual", "kd_topk_kl_backward_residual",
     "kd_teacher_topk_workspace_size", "kd_teacher_topk", "PRODUCER_KERNELS",
     "kd_gemm_bf16_diag", "kd_gemm_bf16_diag_pair", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
-    "KERNELS", "kd_timing_start", "kd_timing_stop", "kd_timing_query", "kd_timing_release",
+    "KERNELS", "SWEEP_KERNELS", "kd_timing_start", "kd_timing_stop", "kd_timing_query", "kd_timing_release",
     "topk_kl_loss",
 ]
 
 # contraction kernel ids of the diagnostic timing interface
 KERNELS = {"logits_fwd": 0, "logits_bwd": 1, "dh": 3, "dW": 4}
+# the single sweep's gradient pass (a SIMT kernel), timed the same way
+SWEEP_KERNELS = {"grad_pass": 7}
 PRODUCER_KERNELS = {"topk_pass1": 5, "topk_scan": 6}
 
 KD_OK = 0
@@ -71,6 +74,10 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_launch_count.argtypes = [i64, i64, i64, i32, i64, ctypes.POINTER(i32),
                                                ctypes.POINTER(i32)]
         L.kd_topk_kl_launch_count.restype = ctypes.c_int
+        L.kd_topk_kl_forward_backward_workspace_size.argtypes = [i64, i64, i64, i32, i64,
+                                                                 ctypes.POINTER(sz),
+                                                                 ctypes.POINTER(i32)]
+        L.kd_topk_kl_forward_backward_workspace_size.restype = ctypes.c_int
         L.kd_topk_kl_forward.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, f32, i64,
                                          vp, vp, vp, vp, vp, sz, vp, vp]
         L.kd_topk_kl_forward.restype = ctypes.c_int
@@ -167,6 +174,15 @@ def kd_topk_kl_launch_count(T: int, V: int, d: int, K: int, chunk: int):
     _check(lib().kd_topk_kl_launch_count(T, V, d, K, chunk, ctypes.byref(f), ctypes.byref(b)),
            "kd_topk_kl_launch_count")
     return f.value, b.value
+
+
+def kd_topk_kl_forward_backward_workspace_size(T: int, V: int, d: int, K: int, chunk: int):
+    """(workspace bytes, kernel launches) of kd_topk_kl_forward_backward."""
+    b, n = ctypes.c_size_t(0), ctypes.c_int32(0)
+    _check(lib().kd_topk_kl_forward_backward_workspace_size(T, V, d, K, chunk, ctypes.byref(b),
+                                                            ctypes.byref(n)),
+           "kd_topk_kl_forward_backward_workspace_size")
+    return b.value, n.value
 
 
 def kd_topk_kl_forward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, loss, lse,
@@ -421,13 +437,18 @@ def topk_kl_loss(h, W, teacher_idx, teacher_logits, valid, tau, chunk=4096):
 
 class TopKKL:
     """Allocates outputs and one workspace (torch) for a fixed shape and runs
-    the library's forward and backward on the current stream."""
+    the library's forward and backward on the current stream.  fused=True sizes
+    the workspace for the one-call training step (forward_backward) as well;
+    otherwise its first forward_backward call allocates that workspace."""
 
-    def __init__(self, T, V, d, K, chunk, device="cuda"):
+    def __init__(self, T, V, d, K, chunk, device="cuda", fused=False):
         self.T, self.V, self.d, self.K, self.chunk = T, V, d, K, chunk
         fwd, bwd = kd_topk_kl_workspace_size(T, V, d, K, chunk)
+        self.sweep_bytes = kd_topk_kl_forward_backward_workspace_size(T, V, d, K, chunk)[0]
         dev = torch.device(device)
-        self.ws = torch.empty(max(fwd, bwd), dtype=torch.uint8, device=dev)
+        nbytes = max(fwd, bwd, self.sweep_bytes) if fused else max(fwd, bwd)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        self._ws_sweep = None
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.loss = torch.empty(1, dtype=torch.float32, device=dev)
         self.lse = torch.empty(T, dtype=torch.float32, device=dev)
@@ -443,10 +464,16 @@ class TopKKL:
 
     def forward_backward(self, h, W, idx, tl, valid, tau, grad_loss=1.0, accumulate_dW=False,
                          row_kl=True, stream=None):
+        ws = self.ws
+        if ws.numel() < self.sweep_bytes:
+            if self._ws_sweep is None:
+                self._ws_sweep = torch.empty(self.sweep_bytes, dtype=torch.uint8,
+                                             device=self.ws.device)
+            ws = self._ws_sweep
         kd_topk_kl_forward_backward(h, W, idx, tl, valid, tau, self.chunk, grad_loss, self.loss,
                                     self.lse, self.dh, self.dW,
                                     self.row_kl if row_kl else None,
-                                    flags=KD_ACCUMULATE_DW if accumulate_dW else 0, ws=self.ws,
+                                    flags=KD_ACCUMULATE_DW if accumulate_dW else 0, ws=ws,
                                     dev_status=self.status, stream=stream)
         return self.loss, self.dh, self.dW
 

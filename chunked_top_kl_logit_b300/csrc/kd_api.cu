@@ -118,6 +118,7 @@ struct Layout {
   size_t nvalid, losspart, sidx, sp, sslot, tterm, resid;  // shared by both passes
   size_t zg, part;                                  // forward
   size_t rowmap, split_info, hc, hct, dz, dhpart;   // backward
+  size_t szg, spart, srowkl;                        // single sweep (sweep layouts only)
   size_t fwd_total, bwd_total;
   int64_t rows_chunk;
   int dh_splits;      // largest split count of the dh contraction
@@ -125,7 +126,11 @@ struct Layout {
   int64_t hct_ld;     // row pitch (elements) of the transposed h chunk
 };
 
-Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
+// sweep: the single-sweep training step's layout, in which the chunk buffer
+// (dz) holds the chunk's fp32 logits (G overwrites them in place) and the
+// forward's tables follow the backward's buffers; bwd_total is its size.
+Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk,
+                   bool sweep = false) {
   Layout L{};
   size_t off = 0;
   L.nvalid = off;   off += 256;
@@ -148,8 +153,13 @@ Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk) {
   L.hc = off;         off += al256(static_cast<size_t>(L.rows_chunk * d) * 2);
   L.hct_ld = cdiv(L.rows_chunk, 8) * 8;  // 16-byte row pitch for the TMA
   L.hct = off;        off += al256(static_cast<size_t>(L.hct_ld * d) * 2);
-  L.dz = off;         off += al256(static_cast<size_t>(L.rows_chunk * V) * 2);
+  L.dz = off;         off += al256(static_cast<size_t>(L.rows_chunk * V) * (sweep ? 4 : 2));
   L.dhpart = off;     off += al256(static_cast<size_t>(L.part_rows * d) * 4);
+  if (sweep) {
+    L.szg = off;      off += al256(static_cast<size_t>(T * K) * 4);
+    L.spart = off;    off += al256(static_cast<size_t>(cdiv(V, ZBN) * L.rows_chunk) * 4);
+    L.srowkl = off;   off += al256(static_cast<size_t>(T) * 4);
+  }
   L.bwd_total = off;
   return L;
 }
@@ -256,7 +266,7 @@ template <int MODE>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                 const CUtensorMap& dm, GemmParams p, int sms, cudaStream_t st) {
   if (p.num_tiles <= 0) return KD_OK;
-  p.epi_smem = (MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX)
+  p.epi_smem = (MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX || MODE == EPI_FWDZ)
                    ? 4u * 2u * DW_PIECE_FLOATS * 4u
                    : 0u;
   // the stage ring shares the opt-in shared-memory limit with the staging
@@ -267,8 +277,10 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c
   static bool attr_ok[64];
   if (!ensure_smem_attr(kd_gemm_kernel<MODE>, attr_once, attr_ok)) return KD_ERR_CUDA;
   const int grid = p.num_tiles < sms ? p.num_tiles : sms;
-  // the residual variant's forward is timed as the forward logit kernel
-  const int slot = MODE == EPI_STORE ? -1 : timing_slot(MODE == EPI_FWD_RESID ? EPI_FWD : MODE);
+  // the residual variant's and the single sweep's forwards are timed as the
+  // forward logit kernel
+  const int slot = MODE == EPI_STORE ? -1
+                   : timing_slot((MODE == EPI_FWD_RESID || MODE == EPI_FWDZ) ? EPI_FWD : MODE);
   if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
     return KD_ERR_CUDA;
   kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, c, dm, p);
@@ -472,6 +484,19 @@ int kd_topk_kl_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K, int64_
   return KD_OK;
 }
 
+int kd_topk_kl_forward_backward_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K,
+                                               int64_t chunk, size_t* bytes, int32_t* launches) {
+  const int rc = check_shape(T, V, d, K, chunk);
+  if (rc != KD_OK) return rc;
+  const Layout L = make_layout(T, V, d, K, chunk, true);
+  if (bytes) *bytes = L.bwd_total;
+  // prep, row order; per chunk: row gather (plain and transposed), logit GEMM,
+  // combine, gradient pass, dh, [dh split reduce], dW; loss partials, loss
+  if (launches)
+    *launches = static_cast<int32_t>(2 + cdiv(T, L.rows_chunk) * (L.dh_splits > 1 ? 8 : 7) + 2);
+  return KD_OK;
+}
+
 int kd_topk_kl_launch_count(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk,
                             int32_t* fwd_launches, int32_t* bwd_launches) {
   const int rc = check_shape(T, V, d, K, chunk);
@@ -523,9 +548,107 @@ int enqueue_forward(const void* h, const void* W, const uint8_t* valid, int64_t 
 
   const int nb = static_cast<int>(cdiv(T, 32));
   kd_combine_kernel<<<nb, dim3(32, COMBINE_SPLIT), 0, st>>>(
-      part, p.n_tiles, static_cast<int>(T), K, w.sidx, w.sp, zg, w.tterm,
+      part, T, p.n_tiles, static_cast<int>(T), K, nullptr, 0, w.sidx, w.sp, zg, w.tterm,
       var.residual() ? w.resid : nullptr, valid, lse, row_kl, var.outside_mass_out, w.losspart);
   kd_loss_final_kernel<<<1, 256, 0, st>>>(w.losspart, nb, w.nvalid, loss);
+  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
+
+// The gradient contractions of one chunk of compacted valid rows [c0, c0 + C)
+// (their count clamp(*nvalid - c0, 0, C) stays on the device), given the
+// chunk's bf16 G (row pitch g_ld elements) and h_c^T: dh rows through the
+// row map, split over V on the device when the chunk has few rows, and dW
+// (accumulate: added to dW instead of stored).
+int enqueue_grad_contractions(const void* W, int64_t V, int64_t d, const Layout& L, const Ws& w,
+                              int sms, const int* rowmap, const __nv_bfloat16* G, int64_t g_ld,
+                              const __nv_bfloat16* hct, float* dhpart, int* split_info,
+                              int64_t c0, float* dh, float* dW, int accumulate,
+                              int32_t* dev_status, cudaStream_t st) {
+  int rc = KD_OK;
+  const int S = L.dh_splits;
+  const int64_t C = L.rows_chunk;
+  CUtensorMap ta, tb;
+  // (2) dh rows of the chunk, computed transposed: dh_c^T = W^T G_c^T, so a
+  // tile is 128 hidden units x 256 chunk rows (A = W as an MN-major operand,
+  // B = G K-major).  The contraction over V is split on the device when the
+  // chunk holds too few rows to fill the GPU.
+  if (!make_map(&ta, W, d, V, d, 64) || !make_map(&tb, G, V, C, g_ld, kGradBN))
+    return KD_ERR_CUDA;
+  GemmParams q = base_params(1, 0, kGradBN);
+  q.m_tiles = static_cast<int>(cdiv(d, BM));
+  q.n_tiles = static_cast<int>(cdiv(C, kGradBN));
+  q.splits = S;
+  q.num_tiles = q.m_tiles * q.n_tiles * S;  // upper bound; the device decides
+  q.k_steps = static_cast<int>(cdiv(V, BK));
+  q.ks_per_split = q.k_steps;
+  q.n_fast = 0;
+  q.group_m = q.m_tiles;                    // hidden-unit tiles fastest: W slabs shared
+  q.M = static_cast<int>(d);
+  q.N = static_cast<int>(C);
+  q.status = dev_status;
+  q.out = dh;
+  q.out2 = dhpart;
+  q.ld_out = d;
+  q.dyn_count = w.nvalid;
+  q.dyn_base = static_cast<int>(c0);
+  q.dyn_cap = static_cast<int>(C);
+  q.dyn_kind = 3;
+  q.rowmap = rowmap;
+  q.rowmap_base = static_cast<int>(c0);
+  q.part_rows = static_cast<int>(L.part_rows);
+  q.policy_sms = kPolicySMs;
+  q.split_info = split_info;
+  if ((rc = launch_gemm<EPI_DH>(ta, tb, ta, ta, q, sms, st))) return rc;
+  if (S > 1) {
+    kd_split_reduce_rows_kernel<<<sms * 4, 256, 0, st>>>(
+        dh, dhpart, split_info, rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
+        static_cast<int>(d / 4));
+    if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+  }
+
+  // (3) dW (+)= G_c^T h_c: tiles of 128 vocabulary rows x BNw hidden units
+  // (A = G as an MN-major operand, B = h_c^T K-major), the contraction over
+  // the chunk's valid rows; 32 x 32 pieces of the tile are stored or
+  // reduce-added into dW by the TMA.
+  const int BNw = dw_tile_width(d);
+  CUtensorMap tc, td;
+  if (!make_map(&ta, G, V, C, g_ld, 64) ||
+      !make_map(&tb, hct, C, d, L.hct_ld, static_cast<uint32_t>(BNw)) ||
+      !make_map_f32(&tc, dW, d, V, d, 32, 32, true) || !make_map_f32(&td, dW, d, V, d, 16, 32))
+    return KD_ERR_CUDA;
+  GemmParams r = base_params(1, 0, BNw);
+  r.m_tiles = static_cast<int>(cdiv(V, BM));
+  r.n_tiles = static_cast<int>(d / BNw);
+  r.num_tiles = r.m_tiles * r.n_tiles;
+  r.k_steps = static_cast<int>(cdiv(C, BK));
+  r.ks_per_split = r.k_steps;
+  r.n_fast = 1;                             // hidden-unit tiles fastest: G slabs shared
+  r.group_m = 1;
+  r.M = static_cast<int>(V);
+  r.N = static_cast<int>(d);
+  r.status = dev_status;
+  r.out = dW;
+  r.out2 = nullptr;
+  r.ld_out = d;
+  r.accumulate = accumulate;
+  r.dyn_count = w.nvalid;
+  r.dyn_base = static_cast<int>(c0);
+  r.dyn_cap = static_cast<int>(C);
+  r.dyn_kind = 2;
+  return launch_gemm<EPI_DW>(ta, tb, tc, td, r, sms, st);
+}
+
+// The chunk's valid rows of h as h_c^T (dW's B operand): hcT[j][i] =
+// h[rowmap[c0 + i]][j] for the chunk's valid rows i, zero up to the pitch.
+int enqueue_gather_t(const void* h, int64_t d, const Layout& L, const Ws& w, const int* rowmap,
+                     int64_t c0, __nv_bfloat16* hct, cudaStream_t st) {
+  const int64_t C = L.rows_chunk;
+  kd_gather_rows_t_kernel<<<dim3(static_cast<unsigned>(cdiv(d, 32)),
+                                 static_cast<unsigned>(cdiv(C, 32))),
+                            dim3(32, 8), 0, st>>>(static_cast<const __nv_bfloat16*>(h), rowmap,
+                                                  w.nvalid, static_cast<int>(c0),
+                                                  static_cast<int>(C), static_cast<int>(L.hct_ld),
+                                                  static_cast<int>(d), hct);
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
@@ -546,7 +669,6 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
   float* dhpart = reinterpret_cast<float*>(wb + L.dhpart);
   int* split_info = reinterpret_cast<int*>(wb + L.split_info);
   const float inv_tau = 1.0f / tau;
-  const int S = L.dh_splits;
   const int64_t C = L.rows_chunk;
 
   // Rows with valid = 0 have an exactly zero gradient: dh starts at zero and
@@ -554,24 +676,18 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
   // order.  Their count stays on the device; every kernel clamps to it.
   if (cudaMemsetAsync(dh, 0, static_cast<size_t>(T * d) * sizeof(float), st) != cudaSuccess)
     return KD_ERR_CUDA;
-  kd_compact_rows_kernel<<<1, 1024, 0, st>>>(valid, static_cast<int>(T), rowmap);
+  kd_compact_rows_kernel<<<1, 1024, 0, st>>>(valid, static_cast<int>(T), nullptr, rowmap);
   if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
 
   for (int64_t c0 = 0; c0 < T; c0 += C) {
     CUtensorMap ta, tb;
-    const int gblocks = sms * 4;
 
     // (0) the chunk's valid rows of h, zero-padded to C rows, and transposed
-    kd_gather_rows_kernel<<<gblocks, 256, 0, st>>>(
+    kd_gather_rows_kernel<<<sms * 4, 256, 0, st>>>(
         static_cast<const uint4*>(h), rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
         static_cast<int>(d / 8), reinterpret_cast<uint4*>(hc));
-    kd_gather_rows_t_kernel<<<dim3(static_cast<unsigned>(cdiv(d, 32)),
-                                   static_cast<unsigned>(cdiv(C, 32))),
-                              dim3(32, 8), 0, st>>>(static_cast<const __nv_bfloat16*>(h), rowmap,
-                                                    w.nvalid, static_cast<int>(c0),
-                                                    static_cast<int>(C), static_cast<int>(L.hct_ld),
-                                                    static_cast<int>(d), hct);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+    if ((rc = enqueue_gather_t(h, d, L, w, rowmap, c0, hct, st))) return rc;
 
     // (1) recompute the chunk's logit tiles and write G as bf16
     if (!make_map(&ta, hc, d, C, d, BM) || !make_map(&tb, W, d, V, d, ZBN)) return KD_ERR_CUDA;
@@ -602,77 +718,113 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
     if (!make_map(&tg, dz, V, C, V, 32)) return KD_ERR_CUDA;
     if ((rc = launch_gemm<EPI_DZ>(ta, tb, tg, ta, p, sms, st))) return rc;
 
-    // (2) dh rows of the chunk, computed transposed: dh_c^T = W^T G_c^T, so a
-    // tile is 128 hidden units x 256 chunk rows (A = W as an MN-major operand,
-    // B = G K-major).  The contraction over V is split on the device when the
-    // chunk holds too few rows to fill the GPU.
-    if (!make_map(&ta, W, d, V, d, 64) || !make_map(&tb, dz, V, C, V, kGradBN))
-      return KD_ERR_CUDA;
-    GemmParams q = base_params(1, 0, kGradBN);
-    q.m_tiles = static_cast<int>(cdiv(d, BM));
-    q.n_tiles = static_cast<int>(cdiv(C, kGradBN));
-    q.splits = S;
-    q.num_tiles = q.m_tiles * q.n_tiles * S;  // upper bound; the device decides
-    q.k_steps = static_cast<int>(cdiv(V, BK));
-    q.ks_per_split = q.k_steps;
-    q.n_fast = 0;
-    q.group_m = q.m_tiles;                    // hidden-unit tiles fastest: W slabs shared
-    q.M = static_cast<int>(d);
-    q.N = static_cast<int>(C);
-    q.status = dev_status;
-    q.out = dh;
-    q.out2 = dhpart;
-    q.ld_out = d;
-    q.dyn_count = w.nvalid;
-    q.dyn_base = static_cast<int>(c0);
-    q.dyn_cap = static_cast<int>(C);
-    q.dyn_kind = 3;
-    q.rowmap = rowmap;
-    q.rowmap_base = static_cast<int>(c0);
-    q.part_rows = static_cast<int>(L.part_rows);
-    q.policy_sms = kPolicySMs;
-    q.split_info = split_info;
-    if ((rc = launch_gemm<EPI_DH>(ta, tb, ta, ta, q, sms, st))) return rc;
-    if (S > 1) {
-      kd_split_reduce_rows_kernel<<<gblocks, 256, 0, st>>>(
-          dh, dhpart, split_info, rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
-          static_cast<int>(d / 4));
-      if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
-    }
-
-    // (3) dW (+)= G_c^T h_c: tiles of 128 vocabulary rows x BNw hidden units
-    // (A = G as an MN-major operand, B = h_c^T K-major), the contraction over
-    // the chunk's valid rows; 32 x 32 pieces of the tile are stored or
-    // reduce-added into dW by the TMA.
-    const int BNw = dw_tile_width(d);
-    CUtensorMap tc, td;
-    if (!make_map(&ta, dz, V, C, V, 64) || !make_map(&tb, hct, C, d, L.hct_ld, static_cast<uint32_t>(BNw)) ||
-        !make_map_f32(&tc, dW, d, V, d, 32, 32, true) || !make_map_f32(&td, dW, d, V, d, 16, 32))
-      return KD_ERR_CUDA;
-    GemmParams r = base_params(1, 0, BNw);
-    r.m_tiles = static_cast<int>(cdiv(V, BM));
-    r.n_tiles = static_cast<int>(d / BNw);
-    r.num_tiles = r.m_tiles * r.n_tiles;
-    r.k_steps = static_cast<int>(cdiv(C, BK));
-    r.ks_per_split = r.k_steps;
-    r.n_fast = 1;                             // hidden-unit tiles fastest: G slabs shared
-    r.group_m = 1;
-    r.M = static_cast<int>(V);
-    r.N = static_cast<int>(d);
-    r.status = dev_status;
-    r.out = dW;
-    r.out2 = nullptr;
-    r.ld_out = d;
-    r.accumulate = (c0 > 0 || accumulate_dW) ? 1 : 0;
-    r.dyn_count = w.nvalid;
-    r.dyn_base = static_cast<int>(c0);
-    r.dyn_cap = static_cast<int>(C);
-    r.dyn_kind = 2;
-    if ((rc = launch_gemm<EPI_DW>(ta, tb, tc, td, r, sms, st))) return rc;
+    // (2), (3) dh and dW of the chunk
+    if ((rc = enqueue_grad_contractions(W, V, d, L, w, sms, rowmap, dz, V, hct, dhpart, split_info,
+                                        c0, dh, dW, (c0 > 0 || accumulate_dW) ? 1 : 0,
+                                        dev_status, st)))
+      return rc;
   }
   return KD_OK;
 }
 
+// The single-sweep training step after the teacher prep (one logit GEMM per
+// row instead of two): rows in the order valid rows, then invalid rows; per
+// chunk of C rows of that order, the forward logit GEMM also stores the
+// chunk's fp32 logits, the combine gives lse and row_kl of its rows, the
+// gradient pass turns the valid rows' logits into bf16 G in place, and the dh
+// and dW contractions follow as in the backward.  The chunks of valid rows are
+// the backward's, and every value is formed by the same operations, so the
+// results equal forward + backward bit for bit (the loss too: its partial sums
+// are formed over the rows in their original order).
+int enqueue_sweep(const void* h, const void* W, const uint8_t* valid, int64_t T, int64_t V,
+                  int64_t d, int32_t K, float tau, const Layout& L, void* ws, const Ws& w,
+                  int sms, float grad_loss, int accumulate_dW, float* loss,
+                  float* lse, float* row_kl, float* dh, float* dW, int32_t* dev_status,
+                  cudaStream_t st) {
+  int rc = KD_OK;
+  char* wb = static_cast<char*>(ws);
+  int* rowmap = reinterpret_cast<int*>(wb + L.rowmap);
+  int* split_info = reinterpret_cast<int*>(wb + L.split_info);
+  __nv_bfloat16* hc = reinterpret_cast<__nv_bfloat16*>(wb + L.hc);
+  __nv_bfloat16* hct = reinterpret_cast<__nv_bfloat16*>(wb + L.hct);
+  float* dhpart = reinterpret_cast<float*>(wb + L.dhpart);
+  float* zg = reinterpret_cast<float*>(wb + L.szg);
+  float* part = reinterpret_cast<float*>(wb + L.spart);
+  float* zbuf = reinterpret_cast<float*>(wb + L.dz);
+  float* rkl = row_kl ? row_kl : reinterpret_cast<float*>(wb + L.srowkl);
+  const float inv_tau = 1.0f / tau;
+  const int64_t C = L.rows_chunk;
+
+  if (cudaMemsetAsync(dh, 0, static_cast<size_t>(T * d) * sizeof(float), st) != cudaSuccess)
+    return KD_ERR_CUDA;
+  kd_compact_rows_kernel<<<1, 1024, 0, st>>>(valid, static_cast<int>(T), w.nvalid, rowmap);
+  if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+
+  for (int64_t c0 = 0; c0 < T; c0 += C) {
+    const int64_t M = (T - c0) < C ? (T - c0) : C;
+    CUtensorMap ta, tb, tz;
+    // (0) the chunk's rows of h in that order, and its valid rows transposed
+    kd_gather_rows_kernel<<<sms * 4, 256, 0, st>>>(
+        static_cast<const uint4*>(h), rowmap, nullptr, static_cast<int>(c0), static_cast<int>(M),
+        static_cast<int>(d / 8), reinterpret_cast<uint4*>(hc));
+    if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+    if ((rc = enqueue_gather_t(h, d, L, w, rowmap, c0, hct, st))) return rc;
+
+    // (1) logit tiles of the chunk: lse partials, gather, fp32 logits stored
+    if (!make_map(&ta, hc, d, M, d, BM) || !make_map(&tb, W, d, V, d, ZBN) ||
+        !make_map_f32(&tz, zbuf, V, M, V, 32, 32, true))
+      return KD_ERR_CUDA;
+    GemmParams p = base_params(0, 0, ZBN);
+    logit_schedule(p, M, V, d);
+    p.status = dev_status;
+    p.K = K;
+    p.sidx = w.sidx;
+    p.sp = w.sp;
+    p.sslot = w.sslot;
+    p.inv_tau = inv_tau;
+    p.c_log2 = LOG2E * inv_tau;
+    p.part_ld = C;
+    p.part = part;
+    p.zg = zg;
+    p.gidx = nullptr;
+    p.nvalid = w.nvalid;
+    p.rowmap = rowmap;
+    p.rowmap_base = static_cast<int>(c0);
+    if ((rc = launch_gemm<EPI_FWDZ>(ta, tb, tz, ta, p, sms, st))) return rc;
+
+    // (2) lse and row_kl of the chunk's rows
+    kd_combine_kernel<<<static_cast<unsigned>(cdiv(M, 32)), dim3(32, COMBINE_SPLIT), 0, st>>>(
+        part, C, p.n_tiles, static_cast<int>(M), K, rowmap, static_cast<int>(c0), w.sidx, w.sp,
+        zg, w.tterm, nullptr, valid, lse, rkl, nullptr, nullptr);
+    if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+
+    // (3) G of the chunk's valid rows, in place over their logits
+    const int slot = timing_slot(KD_KERNEL_GRAD_PASS);
+    if (slot >= 0 &&
+        cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
+      return KD_ERR_CUDA;
+    kd_grad_rows_kernel<<<static_cast<unsigned>(cdiv(C, GRAD_WARPS)), 32 * GRAD_WARPS, 0, st>>>(
+        zbuf, static_cast<int>(V), static_cast<int>(C), rowmap, static_cast<int>(c0),
+        static_cast<int>(M), w.nvalid, w.sidx, w.sp, K, lse, grad_loss, inv_tau,
+        LOG2E * inv_tau);
+    if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+    if (slot >= 0 &&
+        cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
+      return KD_ERR_CUDA;
+
+    // (4) dh and dW of the chunk from G (row pitch 2V bf16 over the logit rows)
+    if ((rc = enqueue_grad_contractions(W, V, d, L, w, sms, rowmap,
+                                        reinterpret_cast<const __nv_bfloat16*>(zbuf), 2 * V, hct,
+                                        dhpart, split_info, c0, dh, dW,
+                                        (c0 > 0 || accumulate_dW) ? 1 : 0, dev_status, st)))
+      return rc;
+  }
+  const int nb = static_cast<int>(cdiv(T, 32));
+  kd_loss_blocks_kernel<<<static_cast<unsigned>(cdiv(nb, 256)), 256, 0, st>>>(
+      rkl, static_cast<int>(T), w.losspart);
+  kd_loss_final_kernel<<<1, 256, 0, st>>>(w.losspart, nb, w.nvalid, loss);
+  return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -739,24 +891,20 @@ int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* tea
   if (!loss || !lse || !dh || !dW || !aligned16(dh) || !aligned16(dW)) return KD_ERR_INVALID_ARG;
   if (!std::isfinite(grad_loss) || (flags & ~static_cast<uint32_t>(KD_ACCUMULATE_DW)))
     return KD_ERR_INVALID_ARG;
-  const Layout L = make_layout(T, V, d, K, chunk);
-  if (ws_bytes < (L.fwd_total > L.bwd_total ? L.fwd_total : L.bwd_total)) return KD_ERR_WORKSPACE;
+  const Layout L = make_layout(T, V, d, K, chunk, true);
+  if (ws_bytes < L.bwd_total) return KD_ERR_WORKSPACE;
   int sms = 0;
   if ((rc = device_sms(&sms)) != KD_OK) return rc;
   if (!encode_fn()) return KD_ERR_CUDA;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const Ws w = carve(ws, L);
-  // one teacher prep serves both passes: the backward's buffers overlay the
-  // forward's lse partials, which the combine has consumed by then
   const Variant var;
   if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
                      st)))
     return rc;
-  if ((rc = enqueue_forward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, loss, lse, row_kl,
-                            nullptr, dev_status, st)))
-    return rc;
-  return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, lse, grad_loss, dh, dW,
-                          (flags & KD_ACCUMULATE_DW) ? 1 : 0, dev_status, st);
+  return enqueue_sweep(h, W, valid, T, V, d, K, tau, L, ws, w, sms, grad_loss,
+                       (flags & KD_ACCUMULATE_DW) ? 1 : 0, loss, lse, row_kl, dh, dW, dev_status,
+                       st);
 }
 
 int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t Kd,

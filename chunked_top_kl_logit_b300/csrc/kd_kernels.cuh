@@ -48,7 +48,9 @@ constexpr float LN2 = 0.6931471805599453f;
 // so that profiles tell them apart.
 // EPI_TMAX: the contraction of the teacher-side top-K producer.
 // EPI_FWD_RESID: the forward of the residual-mass variant, whose lse partials
-// cover only the columns outside the row's cache.
+// cover only the columns outside the row's cache.  EPI_FWDZ: the forward of
+// the single-sweep training step on one chunk of rows (valid rows first),
+// which also stores the chunk's fp32 logits for the gradient pass.
 enum EpiMode {
   EPI_FWD = 0,
   EPI_DZ = 1,
@@ -56,7 +58,8 @@ enum EpiMode {
   EPI_DH = 3,
   EPI_DW = 4,
   EPI_TMAX = 5,
-  EPI_FWD_RESID = 6
+  EPI_FWD_RESID = 6,
+  EPI_FWDZ = 7
 };
 
 struct GemmParams {
@@ -342,15 +345,28 @@ __device__ __forceinline__ uint32_t gather_chunk(const GemmParams& p, const uint
 // EXCL (residual-mass variant): the partial leaves out the cached columns, so
 // that the mass outside the cache is a sum of its own terms, never 1 minus
 // the cached mass.
-template <bool EXCL>
+// STOREZ (single sweep): the launch covers rows rowmap[rowmap_base + local row]
+// of one chunk, valid rows first; the partial goes to part[tile][local row],
+// and warps holding valid rows also store the tile's fp32 logits through the
+// TMA (32 x 32 pieces staged in the 128-byte swizzle, as EPI_TMAX does) into
+// the chunk buffer that the gradient pass reads.
+template <bool EXCL, bool STOREZ>
 __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, const TileCoord& c,
                                         int acc,
                                         uint32_t tmem_row, int r_in_tile, uint64_t* tfull,
                                         uint64_t* tempty, uint32_t use, volatile int* abort_flag,
-                                        bool& ok) {
+                                        bool& ok, const CUtensorMap* tmC, float* stage_buf,
+                                        uint32_t& piece) {
+  const int lane = threadIdx.x & 31;
   const int lrow = c.m * BM + r_in_tile;
   const bool row_ok = lrow < sc_.M;
-  const int64_t grow = static_cast<int64_t>(p.row0) + lrow;
+  int64_t grow = static_cast<int64_t>(p.row0) + lrow;
+  bool zstore = false;
+  if (STOREZ) {
+    grow = row_ok ? p.rowmap[p.rowmap_base + lrow] : 0;
+    const int nvc = min(max(*p.nvalid - p.rowmap_base, 0), sc_.M);
+    zstore = lrow - lane < nvc;  // warp-uniform: the warp's first row is valid
+  }
   const int v0 = c.n * ZBN;
   const int* srow = p.sidx + grow * p.K;
   int pos = p.K;
@@ -372,6 +388,24 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
     uint32_t r[32];
     tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
     tmem_ld_wait(r);
+    if (STOREZ && zstore) {  // warp-uniform
+      float* buf = stage_buf + (piece & 1u) * DW_PIECE_FLOATS;
+      if (lane == 0) bulk_wait_group_read<1>();  // the copy from this buffer two pieces ago is done
+      __syncwarp();
+      float4* b4 = reinterpret_cast<float4*>(buf);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)  // row `lane`, 16-byte chunk j, 128-byte swizzle
+        b4[lane * 8 + (j ^ (lane & 7))] =
+            make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
+                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(tmC, buf, cb, lrow - lane);
+        bulk_commit_group();
+      }
+      ++piece;
+    }
     if (EXCL) {  // gather first, then sum the columns the gather did not hit
       const uint32_t hit = gather_chunk(p, r, cb, grow, srow, pos, nxt);
       float u[32];
@@ -421,7 +455,8 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
   }
   tc_fence_before();
   mbar_arrive(&tempty[acc]);
-  if (row_ok) p.part[static_cast<int64_t>(c.n) * p.part_ld + grow] = (m + lg2f(s)) * LN2;
+  if (row_ok)
+    p.part[static_cast<int64_t>(c.n) * p.part_ld + (STOREZ ? lrow : grow)] = (m + lg2f(s)) * LN2;
 }
 
 // Backward: G = s_t (exp(z/tau - lse) - scatter p) / tau as bf16 into the chunk buffer.
@@ -455,7 +490,10 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
       nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
     }
   }
-  // every column gets a q (1 - R/Q); each cached slot adds (R/Q) q - P
+  // every column gets a q (1 - R/Q); each cached slot adds (R/Q) q - P.  The
+  // residual variant forms a cached column's value directly as s (q - P) at its
+  // first slot: with Q small (the student's mass on the cache near 1) R/Q is
+  // large, and s (1 - R/Q) q + s (R/Q) q would cancel away the digits of s q.
   const float a_row = sc * (1.f - rq);
   bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
   ok = __all_sync(0xffffffffu, w);
@@ -478,7 +516,8 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
     float g[32];
     if (sc != 0.f) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) g[j] = a_row * ex2f(fmaf(__uint_as_float(r[j]), p.c_log2, -lb));
+      for (int j = 0; j < 32; ++j)
+        g[j] = __fmul_rn(a_row, ex2f(fmaf(__uint_as_float(r[j]), p.c_log2, -lb)));
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j) g[j] = 0.f;
@@ -487,15 +526,20 @@ __device__ __forceinline__ void epi_dz(const GemmParams& p, const Sched& sc_, co
     while (__any_sync(0xffffffffu, nxt < ce)) {
       if (nxt < ce) {
         const int j = nxt - cb;
-        float add = -(sc * __ldg(p.sp + grow * p.K + pos));
+        const float add = -__fmul_rn(sc, __ldg(p.sp + grow * p.K + pos));
         if (rq != 0.f) {
           uint32_t bits = 0;
 #pragma unroll
           for (int jj = 0; jj < 32; ++jj) bits = (jj == j) ? r[jj] : bits;
-          add += sc * rq * ex2f(fmaf(__uint_as_float(bits), p.c_log2, -lb));
-        }
+          const float sq = __fmul_rn(sc, ex2f(fmaf(__uint_as_float(bits), p.c_log2, -lb)));
+          const bool first = pos == 0 || __ldg(srow + pos - 1) != nxt;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) g[jj] = (jj == j) ? g[jj] + add : g[jj];
+          for (int jj = 0; jj < 32; ++jj)
+            g[jj] = (jj == j) ? (first ? __fadd_rn(sq, add) : g[jj] + (rq * sq + add)) : g[jj];
+        } else {
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) g[jj] = (jj == j) ? __fadd_rn(g[jj], add) : g[jj];
+        }
         ++pos;
         nxt = pos < p.K ? __ldg(srow + pos) : INT_MAX;
       }
@@ -812,7 +856,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  // [pipeline stages][epilogue staging (EPI_DW, EPI_DZ, EPI_TMAX)][barriers, TMEM slot, abort flag]
+  // [pipeline stages][epilogue staging (EPI_DW, EPI_DZ, EPI_TMAX, EPI_FWDZ)][barriers, TMEM slot,
+  // abort flag]
   float* epi_stage = reinterpret_cast<float*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes +
                                                p.epi_smem);
@@ -871,9 +916,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (MODE == EPI_DW)
         epi_dw(p, sc, c, acc, tmem_row, q, tfull, tempty, use, abort_flag, ok, &tmC, &tmD,
                my_stage, piece);
-      else if (MODE == EPI_FWD || MODE == EPI_FWD_RESID)
-        epi_fwd<MODE == EPI_FWD_RESID>(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use,
-                                       abort_flag, ok);
+      else if (MODE == EPI_FWD || MODE == EPI_FWD_RESID || MODE == EPI_FWDZ)
+        epi_fwd<MODE == EPI_FWD_RESID, MODE == EPI_FWDZ>(p, sc, c, acc, tmem_row, r_in_tile,
+                                                         tfull, tempty, use, abort_flag, ok, &tmC,
+                                                         my_stage, piece);
       else if (MODE == EPI_DZ)
         epi_dz(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok, &tmC,
                my_stage, piece);
@@ -887,7 +933,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
     }
     // the TMA copies this warp issued finish before the CTA leaves
-    if ((MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX) && lane == 0)
+    if ((MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX || MODE == EPI_FWDZ) && lane == 0)
       bulk_wait_group_all();
   }
   tc_fence_before();
@@ -918,7 +964,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 // order) so that the contraction epilogues can walk them tile by tile.
 // teacher_lse == null: p = softmax(teacher_logits / tau) over the K entries
 // (renormalised).  Otherwise p = exp(teacher_logits / tau - teacher_lse) under
-// the teacher's full-vocabulary normaliser and resid = max(0, 1 - sum_k p).
+// the teacher's full-vocabulary normaliser and resid = max(0, 1 - sum_k p),
+// the mass outside the cache (formed without cancellation).
 __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restrict__ tl,
                                const float* __restrict__ teacher_lse,
                                const uint8_t* __restrict__ valid, int T, int K, int V,
@@ -940,17 +987,12 @@ __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restr
   m = warp_max(m);
   if (__any_sync(0xffffffffu, bad) && lane == 0) set_status(status, KD_ERR_INDEX_RANGE);
   float L = 0.f;     // full-vocabulary normaliser (teacher_lse given)
-  float logS = 0.f;  // log sum_k exp(a_k - m) (renormalised top-K)
-  if (teacher_lse) {
-    L = teacher_lse[row];
-  } else {
-    float S = 0.f;
-    for (int k = lane; k < K; k += 32) S += expf(tr[k] * inv_tau - m);
-    S = warp_sum(S);
-    logS = logf(S);
-  }
+  float S = 0.f;
+  for (int k = lane; k < K; k += 32) S += expf(tr[k] * inv_tau - m);
+  S = warp_sum(S);
+  const float logS = logf(S);  // log sum_k exp(a_k - m): the cached entries' normaliser
+  if (teacher_lse) L = teacher_lse[row];
   float tt = 0.f;
-  float psum = 0.f;
   int* so = sidx + static_cast<int64_t>(row) * K;
   float* po = sp + static_cast<int64_t>(row) * K;
   int16_t* lo = sslot + static_cast<int64_t>(row) * K;
@@ -958,7 +1000,6 @@ __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restr
     const float lp = teacher_lse ? tr[k] * inv_tau - L : tr[k] * inv_tau - m - logS;
     const float pk = expf(lp);
     if (pk > 0.f) tt += pk * lp;
-    psum += pk;
     const int v = ir[k];
     int rank = 0;
     for (int j = 0; j < K; ++j) {
@@ -970,10 +1011,11 @@ __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restr
     lo[rank] = static_cast<int16_t>(k);
   }
   tt = warp_sum(tt);
-  psum = warp_sum(psum);
   if (lane == 0) {
     tterm[row] = tt;
-    if (resid) resid[row] = teacher_lse ? fmaxf(0.f, 1.f - psum) : 0.f;
+    // 1 - sum_k p = 1 - exp(lseK - L) with lseK = m + log S, formed by expm1 so
+    // that a teacher with nearly all its mass in the cache keeps R's digits
+    if (resid) resid[row] = teacher_lse ? fmaxf(0.f, -expm1f(m + logS - L)) : 0.f;
     if (valid[row]) atomicAdd(nvalid, 1);
   }
 }
@@ -991,6 +1033,9 @@ __global__ void kd_prep_kernel(const int* __restrict__ idx, const float* __restr
 // Q = exp(Lu - lse), less the mass of repeated slots (each slot is its own
 // outcome), with no 1 - sum cancellation; it goes to outside_mass_out (if
 // given) and row_kl gains R (log R - log Q) for R > 0.
+// rowmap != null (single sweep): the launch covers the T rows
+// rowmap[rowmap_base + i] of one chunk, whose partials sit at part[tile][i]
+// (part_ld = the chunk's row capacity); losspart may then be null.
 constexpr int COMBINE_SPLIT = 8;
 
 __device__ __forceinline__ void online_lse_add(float v, float& m, float& s) {
@@ -1017,7 +1062,8 @@ __device__ __forceinline__ float merge_lse(const float (&sm)[COMBINE_SPLIT][32],
 }
 
 __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
-    kd_combine_kernel(const float* __restrict__ part, int n_tiles, int T, int K,
+    kd_combine_kernel(const float* __restrict__ part, int64_t part_ld, int n_tiles, int T, int K,
+                      const int* __restrict__ rowmap, int rowmap_base,
                       const int* __restrict__ sidx, const float* __restrict__ sp,
                       const float* __restrict__ zg, const float* __restrict__ tterm,
                       const float* __restrict__ resid, const uint8_t* __restrict__ valid,
@@ -1028,15 +1074,16 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
   __shared__ float sa[COMBINE_SPLIT][32], smass[COMBINE_SPLIT][32];
   __shared__ double red[32];
   const int x = threadIdx.x, y = threadIdx.y;
-  const int row = blockIdx.x * 32 + x;
-  const bool in = row < T;
+  const int li = blockIdx.x * 32 + x;  // row of this launch
+  const bool in = li < T;
+  const int row = (in && rowmap) ? rowmap[rowmap_base + li] : li;
   const int64_t rk0 = static_cast<int64_t>(row) * K;
   // online logsumexp over this thread's tiles
   float m = -CUDART_INF_F;
   float s = 0.f;
   if (in)
     for (int j = y; j < n_tiles; j += COMBINE_SPLIT)
-      online_lse_add(part[static_cast<int64_t>(j) * T + row], m, s);
+      online_lse_add(part[static_cast<int64_t>(j) * part_ld + li], m, s);
   sm[y][x] = m;
   ss[y][x] = s;
   __syncthreads();
@@ -1107,11 +1154,27 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
     red[x] = kl;
   }
   __syncthreads();
-  if (y == 0 && x == 0) {
+  if (y == 0 && x == 0 && losspart) {
     double t = 0.0;
     for (int i = 0; i < 32; ++i) t += red[i];
     losspart[blockIdx.x] = t;
   }
+}
+
+// Per block of 32 consecutive rows, the double sum of row_kl in row order:
+// the partials the combine forms when it runs over all rows in order (the
+// single sweep's combine runs chunk by chunk in another row order), so that
+// kd_loss_final_kernel gives the same loss bit for bit.
+__global__ void kd_loss_blocks_kernel(const float* __restrict__ row_kl, int T,
+                                      double* __restrict__ losspart) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b * 32 >= T) return;
+  double t = 0.0;
+  for (int i = 0; i < 32; ++i) {
+    const int r = b * 32 + i;
+    t += r < T ? static_cast<double>(row_kl[r]) : 0.0;
+  }
+  losspart[b] = t;
 }
 
 // Single block: fixed-order sum of the per-block partials, divided by N_valid.
@@ -1133,9 +1196,11 @@ __global__ void kd_loss_final_kernel(const double* __restrict__ losspart, int nb
 }
 
 // Valid rows in ascending order: rowmap[i] = the i-th row with valid != 0.
+// nvalid != null (the valid-row count): the invalid rows follow, also in
+// ascending order, rowmap[*nvalid + j] = the j-th row with valid == 0.
 // One block; fixed order, so the compaction is deterministic.
 __global__ void kd_compact_rows_kernel(const uint8_t* __restrict__ valid, int T,
-                                       int* __restrict__ rowmap) {
+                                       const int* __restrict__ nvalid, int* __restrict__ rowmap) {
   __shared__ int warp_incl[32];
   __shared__ int base;
   const int lane = threadIdx.x & 31;
@@ -1164,8 +1229,11 @@ __global__ void kd_compact_rows_kernel(const uint8_t* __restrict__ valid, int T,
       if (lane < nw) warp_incl[lane] = v;
     }
     __syncthreads();
-    const int excl = base + (w > 0 ? warp_incl[w - 1] : 0) + x - f;
-    if (f) rowmap[excl] = t;
+    const int excl = base + (w > 0 ? warp_incl[w - 1] : 0) + x - f;  // valid rows before t
+    if (f)
+      rowmap[excl] = t;
+    else if (nvalid && t < T)
+      rowmap[*nvalid + (t - excl)] = t;
     __syncthreads();
     if (threadIdx.x == 0) base += warp_incl[nw - 1];
     __syncthreads();
@@ -1173,11 +1241,12 @@ __global__ void kd_compact_rows_kernel(const uint8_t* __restrict__ valid, int T,
 }
 
 // Chunk of compacted rows: hc[i] = h[rowmap[c0 + i]] for i < rows and 0 for
-// rows <= i < cap, with rows = clamp(*nvalid - c0, 0, cap).  d8 = d / 8.
+// rows <= i < cap, with rows = clamp(*nvalid - c0, 0, cap), or rows = cap when
+// nvalid is null.  d8 = d / 8.
 __global__ void kd_gather_rows_kernel(const uint4* __restrict__ h, const int* __restrict__ rowmap,
                                       const int* __restrict__ nvalid, int c0, int cap, int d8,
                                       uint4* __restrict__ hc) {
-  const int rows = max(0, min(*nvalid - c0, cap));
+  const int rows = nvalid ? max(0, min(*nvalid - c0, cap)) : cap;
   const int64_t n = static_cast<int64_t>(cap) * d8;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -1215,6 +1284,109 @@ __global__ void kd_gather_rows_t_kernel(const __nv_bfloat16* __restrict__ h,
     const int j = j0 + ty + 8 * r;
     const int i = i0 + tx;
     if (j < d && i < cap) hcT[static_cast<int64_t>(j) * ld + i] = tile[tx][ty + 8 * r];
+  }
+}
+
+// Gradient pass of the single sweep: G for the chunk's valid rows from the
+// fp32 logits the forward stored, G = s (exp(z/tau - lse) - scatter p) / tau
+// with s = g / N_valid (every row here is valid), rounded to bf16 and written
+// in place over the logits.  Row i of the buffer holds z_i (V floats, 4V bytes
+// apart) and receives G_i in its first 2V bytes, so G rows are 2V bf16
+// elements apart.  One warp per row walks it in blocks of GRAD_U x 256
+// columns: every lane loads its 8-column groups of the block, the warp
+// synchronises, then each lane writes G for its groups.  Those G bytes cover
+// only columns the warp has already loaded (column c of G overlays logit c/2),
+// so no lane overwrites a logit that another lane still needs.  The cached
+// entries are walked in ascending order and subtracted from the owning lane's
+// value one slot at a time, the same operations in the same order as the
+// recompute epilogue (EPI_DZ), each product and sum explicitly rounded (never
+// contracted into an FMA by the compiler, which could do so in one kernel and
+// not the other), so G is bit-identical to the split backward's.
+// Rows from the valid count up to the next multiple of 64 (within the buffer's
+// buf_rows) get G = 0: the dW contraction reads whole 64-row steps of G
+// against zero rows of h_c^T, and the stale bytes there (logits of invalid
+// rows, or an earlier chunk's) could hold NaN patterns, which 0 would not
+// cancel.
+constexpr int GRAD_WARPS = 8;
+constexpr int GRAD_U = 4;
+
+__global__ void __launch_bounds__(32 * GRAD_WARPS)
+    kd_grad_rows_kernel(float* __restrict__ zbuf, int V, int buf_rows,
+                        const int* __restrict__ rowmap, int c0, int cap,
+                        const int* __restrict__ nvalid, const int* __restrict__ sidx,
+                        const float* __restrict__ sp, int K, const float* __restrict__ lse,
+                        float grad_loss, float inv_tau, float c_log2) {
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * GRAD_WARPS + (threadIdx.x >> 5);
+  const int nv = *nvalid;
+  const int rows = max(0, min(nv - c0, cap));
+  float* z = zbuf + static_cast<int64_t>(i) * V;
+  uint4* g = reinterpret_cast<uint4*>(z);  // 8 bf16 per uint4
+  if (i >= rows) {  // whole warp
+    if (i < min(buf_rows, (rows + 63) & ~63))
+      for (int col = 8 * lane; col < V; col += 256) g[col >> 3] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const int64_t t = rowmap[c0 + i];
+  const float sc = grad_loss / static_cast<float>(nv) * inv_tau;
+  const float lb = lse[t] * LOG2E;
+  const int* srow = sidx + t * K;
+  const float* prow = sp + t * K;
+  int pos = 0;
+  int nxt = __ldg(srow);
+  for (int b0 = 0; b0 < V; b0 += GRAD_U * 256) {
+    float4 v[GRAD_U][2];
+#pragma unroll
+    for (int u = 0; u < GRAD_U; ++u) {
+      const int col = b0 + u * 256 + 8 * lane;
+      if (col < V) {  // V % 8 == 0: a group is wholly inside or outside
+        v[u][0] = __ldcs(reinterpret_cast<const float4*>(z + col));
+        v[u][1] = __ldcs(reinterpret_cast<const float4*>(z + col) + 1);
+      } else {
+        v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    __syncwarp();  // every lane's loads of this block precede any write below
+    float gg[GRAD_U][8];
+#pragma unroll
+    for (int u = 0; u < GRAD_U; ++u) {
+      const float zz[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
+                           v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        gg[u][j] = sc != 0.f ? __fmul_rn(sc, ex2f(fmaf(zz[j], c_log2, -lb))) : 0.f;
+    }
+    const int be = b0 + GRAD_U * 256;
+    while (nxt < be) {  // warp-uniform: every lane walks the same row
+      const int off = nxt - b0;
+      const int uu = off >> 8, ln = (off >> 3) & 31, jj = off & 7;
+      const float add = -__fmul_rn(sc, __ldg(prow + pos));
+      if (lane == ln) {
+#pragma unroll
+        for (int u = 0; u < GRAD_U; ++u)
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            gg[u][j] = (u == uu && j == jj) ? __fadd_rn(gg[u][j], add) : gg[u][j];
+      }
+      ++pos;
+      nxt = pos < K ? __ldg(srow + pos) : INT_MAX;
+    }
+#pragma unroll
+    for (int u = 0; u < GRAD_U; ++u) {
+      const int col = b0 + u * 256 + 8 * lane;
+      if (col < V) {
+        uint4 pk;
+        __nv_bfloat162 b0v = __floats2bfloat162_rn(gg[u][0], gg[u][1]);
+        __nv_bfloat162 b1v = __floats2bfloat162_rn(gg[u][2], gg[u][3]);
+        __nv_bfloat162 b2v = __floats2bfloat162_rn(gg[u][4], gg[u][5]);
+        __nv_bfloat162 b3v = __floats2bfloat162_rn(gg[u][6], gg[u][7]);
+        pk.x = *reinterpret_cast<uint32_t*>(&b0v);
+        pk.y = *reinterpret_cast<uint32_t*>(&b1v);
+        pk.z = *reinterpret_cast<uint32_t*>(&b2v);
+        pk.w = *reinterpret_cast<uint32_t*>(&b3v);
+        g[col >> 3] = pk;
+      }
+    }
   }
 }
 

@@ -142,19 +142,35 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
 
 /*
  * Forward and backward in one call, for a training step (the aipuls.nl
- * "Summary" describes the loss as the student's training objective): the
- * same results as kd_topk_kl_forward followed by kd_topk_kl_backward with the
- * same arguments, with one teacher prep serving both passes.
+ * "Summary" describes the loss as the student's training objective, computed
+ * chunk by chunk with memory bounded by one chunk): the same results, bit for
+ * bit, as kd_topk_kl_forward followed by kd_topk_kl_backward with the same
+ * arguments, in a single sweep that computes each row's logits once instead
+ * of twice.  Rows are taken in the order valid rows, then invalid rows; per
+ * chunk of `chunk` rows of that order the logit GEMM forms the lse partials
+ * and the gather and also stores the chunk's fp32 logits (chunk x V x 4 bytes
+ * of workspace, the only buffer whose size depends on V times a row count),
+ * the chunk's lse and row_kl follow, a gradient pass turns the valid rows'
+ * stored logits into the bf16 G in place, and the dh and dW contractions
+ * consume it.  No T x V buffer exists at any time.
  *
  * grad_loss: d(objective)/d(loss), as in kd_topk_kl_backward.
  * flags: 0 or KD_ACCUMULATE_DW.  With KD_ACCUMULATE_DW, dW += G^T h instead of
  *   dW = G^T h (gradient accumulation over micro-batches); dh is always
  *   overwritten.
  * Outputs (device): loss, lse (required), row_kl (or NULL), dh, dW.
- * ws/ws_bytes: at least max(*fwd_bytes, *bwd_bytes) of
- *   kd_topk_kl_workspace_size.
+ * ws/ws_bytes: at least *bytes of kd_topk_kl_forward_backward_workspace_size.
  */
 #define KD_ACCUMULATE_DW 1u
+/*
+ * Workspace bytes (*bytes) and number of kernel launches (*launches, the
+ * status/counter resets and the dh zeroing are cudaMemsetAsync calls and are
+ * not counted) of kd_topk_kl_forward_backward at this shape; either pointer
+ * may be NULL.  About chunk * (4 V + 4 d) bytes plus O(T K) tables.
+ * Host-only; KD_ERR_INVALID_ARG / KD_ERR_UNSUPPORTED on bad shapes.
+ */
+int kd_topk_kl_forward_backward_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K,
+                                               int64_t chunk, size_t* bytes, int32_t* launches);
 int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* teacher_idx,
                                 const float* teacher_logits, const uint8_t* valid, int64_t T,
                                 int64_t V, int64_t d, int32_t K, float tau, int64_t chunk,
@@ -322,7 +338,14 @@ int kd_pipeline_wait_selftest(uint64_t limit_ns, int32_t* dev_status, struct CUs
  * The library calls no cudaMalloc, cudaFree or other allocating routine here.
  *
  * - Every GPU that loads the library holds the 32 MiB array until the process
- *   exits.
+ *   exits.  The array belongs to the library's device module, and CUDA
+ *   reserves it when it loads that module on a device.  With lazy module
+ *   loading (CUDA's default) that happens on the first use of any of the
+ *   library's kernels or of the array on that device, which may be this
+ *   entry's first call: that load reserves the array and the kernel images,
+ *   and may synchronise.  A caller that must not see either during its steady
+ *   state makes one warm-up call (this entry or any other library call) on
+ *   each device at start-up.
  * - The first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current) and caches it; make that
  *   first call before any stream capture.
@@ -346,12 +369,15 @@ int kd_topk_kl_forward_noalloc(const void* h, const void* W, const int32_t* teac
  *   KD_KERNEL_TOPK_PASS1  teacher top-K producer: logits, tile maxima, lse partials
  *   KD_KERNEL_TOPK_SCAN   teacher top-K producer: candidate scan of the stored
  *                         logits (a SIMT kernel, timed the same way)
+ *   KD_KERNEL_GRAD_PASS   single sweep (kd_topk_kl_forward_backward): G from the
+ *                         stored logits (a SIMT kernel); that entry's logit GEMM
+ *                         is timed as KD_KERNEL_LOGITS_FWD
  *
  * kd_timing_start(capacity): creates 2 x capacity CUDA events on the current
  *   device (no device memory is allocated) and starts recording: from then on
  *   every launch of an id above that the entry points make (the contractions
- *   of the loss entries and of kd_teacher_topk, and the producer's candidate
- *   scan), from any host thread, is bracketed by an event pair recorded on its
+ *   of the loss entries and of kd_teacher_topk, the producer's candidate scan
+ *   and the single sweep's gradient pass), from any host thread, is bracketed by an event pair recorded on its
  *   stream, until `capacity` launches have been recorded.  Restarting discards
  *   earlier records.
  * kd_timing_stop(): stops recording; the records stay readable.
@@ -366,7 +392,8 @@ enum {
   KD_KERNEL_DH = 3,
   KD_KERNEL_DW = 4,
   KD_KERNEL_TOPK_PASS1 = 5,
-  KD_KERNEL_TOPK_SCAN = 6
+  KD_KERNEL_TOPK_SCAN = 6,
+  KD_KERNEL_GRAD_PASS = 7
 };
 int kd_timing_start(int32_t capacity);
 int kd_timing_stop(void);

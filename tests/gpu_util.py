@@ -39,6 +39,24 @@ def oracle_inputs(x: dict) -> dict:
                 valid=x["valid"].cpu().numpy(), tau=float(x["tau"]))
 
 
+def run_sweep(x: dict, chunk: int, grad_loss: float = 1.0):
+    """The one-call training step (kd_topk_kl_forward_backward, the single
+    sweep) through the library; returns numpy outputs."""
+    g = to_device(x)
+    T, d = g["h"].shape
+    V = g["W"].shape[0]
+    K = g["teacher_idx"].shape[1]
+    m = kd.TopKKL(T, V, d, K, chunk, fused=True)
+    m.forward_backward(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"],
+                       g["tau"], grad_loss)
+    torch.cuda.synchronize()
+    out = dict(status=int(m.status.item()), loss=float(m.loss.item()),
+               lse=m.lse.double().cpu().numpy(), row_kl=m.row_kl.double().cpu().numpy(),
+               dh=m.dh.double().cpu().numpy(), dW=m.dW.double().cpu().numpy())
+    del m
+    return out
+
+
 def run_gpu(x: dict, chunk: int, grad_loss: float = 1.0, backward: bool = True):
     """Forward (+ backward) through the library; returns numpy outputs."""
     g = to_device(x)

@@ -151,9 +151,29 @@ def test_forward_backward_argument_checks():
     L = kd.lib()
     args = lambda flags, lse, ws_bytes: (A, A, A, A, A, T, V, d, K, 1.0, chunk, 1.0, flags,
                                          A, lse, None, A, A, A, ws_bytes, A, None)
-    assert L.kd_topk_kl_forward_backward(*args(2, A, max(f, b))) == INVALID
-    assert L.kd_topk_kl_forward_backward(*args(0, None, max(f, b))) == INVALID
-    assert L.kd_topk_kl_forward_backward(*args(0, A, min(f, b) - 1)) == WORKSPACE
+    sw, _ = kd.kd_topk_kl_forward_backward_workspace_size(T, V, d, K, chunk)
+    assert L.kd_topk_kl_forward_backward(*args(2, A, sw)) == INVALID
+    assert L.kd_topk_kl_forward_backward(*args(0, None, sw)) == INVALID
+    assert L.kd_topk_kl_forward_backward(*args(0, A, sw - 1)) == WORKSPACE
+
+
+def test_forward_backward_workspace_and_launch_count():
+    """The single sweep holds one chunk of fp32 logits (G is written over
+    them) besides the backward's buffers minus its bf16 G chunk, and makes
+    2 + chunks x (7 or 8) + 2 launches."""
+    T, V, d, K = 32768, 201088, 2880, 100
+    for chunk in (4096, 8192):
+        f, b = kd.kd_topk_kl_workspace_size(T, V, d, K, chunk)
+        sw, n = kd.kd_topk_kl_forward_backward_workspace_size(T, V, d, K, chunk)
+        extra = sw - b
+        # + chunk x V x 2 bytes of logits beyond the bf16 G, + O(T K + T V / 256 chunk / T)
+        assert chunk * V * 2 <= extra <= chunk * V * 2 + T * K * 4 + 786 * chunk * 4 + T * 4 + 4096
+        chunks = -(-T // chunk)
+        assert n in (2 + chunks * 7 + 2, 2 + chunks * 8 + 2)
+    with pytest.raises(kd.KDError):
+        kd.kd_topk_kl_forward_backward_workspace_size(0, V, d, K, 64)
+    with pytest.raises(kd.KDError):
+        kd.kd_topk_kl_forward_backward_workspace_size(T, 1020, d, K, 64)
 
 
 def test_residual_entry_argument_checks():

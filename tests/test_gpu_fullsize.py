@@ -10,6 +10,8 @@ the headline workload): the oracle's full forward gives the exact loss and the
 lse and row_kl of every row; dh is compared on seeded rows and dW on seeded
 vocabulary rows, both computed by the oracle from its own lse; the gathered
 indices are compared in full.  Nothing the oracle uses comes from the GPU.
+At ctx_32k the one-call training step (the single sweep the benchmark times)
+must also equal the separate forward and backward bit for bit.
 
 The oracle's row blocks are larger here than its defaults only to make fewer,
 larger BLAS calls; a block is the plain definition applied to a set of rows.
@@ -20,8 +22,8 @@ import pytest
 
 from oracle import kd_oracle as O
 from synth import make_inputs, workload
-from tests.gpu_util import (GRAD_RL2, LSE_ATOL, assert_forward_parity, oracle_inputs, rel_l2,
-                            run_gpu)
+from tests.gpu_util import (GRAD_RL2, LOSS_RTOL, LSE_ATOL, assert_forward_parity,
+                            oracle_inputs, rel_l2, run_gpu, run_sweep)
 
 pytestmark = pytest.mark.gpu
 
@@ -115,6 +117,11 @@ def test_ctx_32k_full_forward_sampled_grads():
     gpu = run_gpu(x, w.chunk)
     assert_forward_parity(gpu, f)
     assert gpu["bwd_status"] == 0
+    sw = run_sweep(x, w.chunk)
+    assert sw["status"] == 0
+    for k in ("loss", "lse", "row_kl", "dh", "dW"):
+        np.testing.assert_array_equal(sw[k], gpu[k], err_msg=k)
+    del sw
     rows, vrows = _sampled_grads(w, gpu, P, f, seed=2, n_rows=512, n_vrows=640, slab=256)
     assert len(rows) >= 500 and len(vrows) >= 1024
     # every row of G sums to zero, so the column sums of dW vanish up to the
@@ -122,4 +129,20 @@ def test_ctx_32k_full_forward_sampled_grads():
     col = gpu["dW"].sum(axis=0)
     assert np.linalg.norm(col) <= 1e-2 * np.linalg.norm(gpu["dW"])
     assert np.all(np.isfinite(gpu["dW"]))
+
+
+def test_ctx_32k_single_sweep_chunk_4096():
+    """The one-call training step at ctx_32k with 4096-row chunks: bit for bit
+    the separate forward and backward at the same chunk size, and held to the
+    oracle's full forward and its sampled gradients."""
+    w, x, P, f = _inputs_and_forward("ctx_32k")
+    sw = run_sweep(x, 4096)
+    assert sw["status"] == 0
+    gpu = run_gpu(x, 4096)
+    for k in ("loss", "lse", "row_kl", "dh", "dW"):
+        np.testing.assert_array_equal(sw[k], gpu[k], err_msg=k)
+    assert abs(sw["loss"] - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert np.abs(sw["lse"] - f["lse"]).max() <= LSE_ATOL
+    assert np.abs(sw["row_kl"] - f["row_kl"]).max() <= LSE_ATOL
+    _sampled_grads(w, sw, P, f, seed=3, n_rows=256, n_vrows=512, slab=128)
     _cache.clear()
