@@ -1,10 +1,12 @@
 #!/usr/bin/env python
 """Benchmark of the fused top-K KL distillation loss, forward + backward.
 
-One step = kd_topk_kl_forward + kd_topk_kl_backward over one synthetic batch
-(every step of the loss: teacher prep, logit GEMM with online lse + gather,
-combine, and per row chunk the logit recompute with the gradient epilogue, dh
-and dW contractions).  Default workload: ctx_32k (T=32768, V=201088, d=2880,
+One step = one kd_topk_kl_forward_backward call over one synthetic batch (the
+single-sweep training step: teacher prep, then per row chunk the logit GEMM with
+online lse + gather that also stores the chunk's fp32 logits, the combine, the
+gradient pass, the dh and dW contractions); `--api split` times
+kd_topk_kl_forward + kd_topk_kl_backward instead (the backward recomputes the
+logits).  Default workload: ctx_32k (T=32768, V=201088, d=2880,
 K=100, tau=1, 10% rows masked), inputs resident in HBM and larger than L2.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl reference]
@@ -360,9 +362,9 @@ def run_ours(args, w, world, rank, local_rank):
     base_alloc = torch.cuda.memory_allocated(dev)
     torch.cuda.reset_peak_memory_stats(dev)
     free_before = torch.cuda.mem_get_info(dev)[0]  # cross-check with the CUDA device's free-memory count
-    fused = args.api == "fused"
     residual = args.variant == "residual"
-    m = kd.TopKKL(T, V, d, K, chunk, device=dev, fused=fused and not residual)
+    fused = args.api == "fused" and not residual  # the residual variant has split entries only
+    m = kd.TopKKL(T, V, d, K, chunk, device=dev, fused=fused)
     if residual:
         from synth import teacher_full_lse
         tlse = teacher_full_lse(x["teacher_logits"].cpu(), tau, seed=args.seed + rank).to(dev)
@@ -406,7 +408,7 @@ def run_ours(args, w, world, rank, local_rank):
     n = args.steps
     fl, bl = kd.kd_topk_kl_launch_count(T, V, d, K, chunk)
     sweep_launches = kd.kd_topk_kl_forward_backward_workspace_size(T, V, d, K, chunk)[1]
-    step_launches = sweep_launches if fused and not residual else fl + bl
+    step_launches = sweep_launches if fused else fl + bl
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
     barrier(world)
     torch.cuda.synchronize()
@@ -446,7 +448,7 @@ def run_ours(args, w, world, rank, local_rank):
 
 
     peaks, peak_src = load_peaks()
-    sweep = fused and not residual
+    sweep = fused
     flops_nominal = 8.0 * T * d * V
     # the single sweep forms each row's logits once: no recompute GEMM
     flops_alg = (2.0 * T + (4.0 if sweep else 6.0) * n_valid) * d * V
@@ -468,7 +470,7 @@ def run_ours(args, w, world, rank, local_rank):
         "tflops_algorithmic": flops_alg / (ms_per_step / 1e3) / 1e12,
         "frac_bf16_peak_burst": tf_nominal / world / burst,
         "frac_bf16_peak_sustained": tf_nominal / world / sustained,
-        "api": args.api, "variant": args.variant,
+        "api": "fused" if fused else "split", "variant": args.variant,
         "fwd_ms": None if fused else fwd_ms, "bwd_ms": None if fused else bwd_ms,
         "kernels": kernels,
         "roofline": {"kernel": f"kd_gemm_kernel<{dom_id}> ({dom_desc})",
@@ -649,9 +651,10 @@ def main(argv=None):
     ap.add_argument("--variant", default="main", choices=["main", "residual"],
                     help="main: teacher renormalised over its top-K; residual: the teacher's "
                          "full-vocabulary normaliser and an 'everything else' outcome")
-    ap.add_argument("--api", default="split", choices=["split", "fused"],
-                    help="split: kd_topk_kl_forward + kd_topk_kl_backward per step; "
-                         "fused: one kd_topk_kl_forward_backward call per step")
+    ap.add_argument("--api", default="fused", choices=["split", "fused"],
+                    help="fused: one kd_topk_kl_forward_backward call per step (the single "
+                         "sweep, each row's logits formed once); split: kd_topk_kl_forward + "
+                         "kd_topk_kl_backward per step (the backward recomputes the logits)")
     ap.add_argument("--cpu-rows", type=int, default=1024)
     ap.add_argument("--ref-rows", type=int, default=256)
     args = ap.parse_args(argv)

@@ -1287,54 +1287,60 @@ __global__ void kd_gather_rows_t_kernel(const __nv_bfloat16* __restrict__ h,
   }
 }
 
-// Gradient pass of the single sweep: G for the chunk's valid rows from the
-// fp32 logits the forward stored, G = s (exp(z/tau - lse) - scatter p) / tau
-// with s = g / N_valid (every row here is valid), rounded to bf16 and written
-// in place over the logits.  Row i of the buffer holds z_i (V floats, 4V bytes
-// apart) and receives G_i in its first 2V bytes, so G rows are 2V bf16
-// elements apart.  One warp per row walks it in blocks of GRAD_U x 256
-// columns: every lane loads its 8-column groups of the block, the warp
-// synchronises, then each lane writes G for its groups.  Those G bytes cover
-// only columns the warp has already loaded (column c of G overlays logit c/2),
-// so no lane overwrites a logit that another lane still needs.  The cached
-// entries are walked in ascending order and subtracted from the owning lane's
-// value one slot at a time, the same operations in the same order as the
-// recompute epilogue (EPI_DZ), each product and sum explicitly rounded (never
-// contracted into an FMA by the compiler, which could do so in one kernel and
-// not the other), so G is bit-identical to the split backward's.
-// Rows from the valid count up to the next multiple of 64 (within the buffer's
-// buf_rows) get G = 0: the dW contraction reads whole 64-row steps of G
-// against zero rows of h_c^T, and the stale bytes there (logits of invalid
-// rows, or an earlier chunk's) could hold NaN patterns, which 0 would not
-// cancel.
+// Gradient pass of the single sweep: G for the valid rows of one sub-chunk
+// (rowmap[s0 + i], i < its row count) from the fp32 logits the forward stored
+// (z row i, V floats), G = s (exp(z/tau - lse) - scatter p) / tau with
+// s = g / N_valid (every row here is valid), rounded to bf16 into row
+// g_row0 + i of the chunk's G buffer (V elements a row).  One warp per
+// GRAD_SEG columns of a row (so that a sub-chunk of a few thousand rows still
+// keeps every SM's memory pipes full), GRAD_U x 256 columns at a time, 8 per
+// lane.  The cached entries are walked
+// in ascending order and subtracted from the owning lane's value one slot at
+// a time, the same operations in the same order as the recompute epilogue
+// (EPI_DZ), each product and sum explicitly rounded (never contracted into an
+// FMA by the compiler, which could do so in one kernel and not the other), so
+// G is bit-identical to the split backward's.
+// Chunk rows from the chunk's valid count up to the next multiple of 64
+// (within the buffer's c_cap rows) get G = 0: the dW contraction reads whole
+// 64-row steps of G against zero rows of h_c^T, and stale bytes there could
+// hold NaN patterns, which 0 would not cancel.  Warps past the sub-chunk's
+// valid rows take those rows (the grid of a chunk's last sub-chunk reaches
+// c_cap).
 constexpr int GRAD_WARPS = 8;
 constexpr int GRAD_U = 4;
+constexpr int GRAD_SEG = 16 * GRAD_U * 256;  // columns per warp
 
 __global__ void __launch_bounds__(32 * GRAD_WARPS)
-    kd_grad_rows_kernel(float* __restrict__ zbuf, int V, int buf_rows,
-                        const int* __restrict__ rowmap, int c0, int cap,
-                        const int* __restrict__ nvalid, const int* __restrict__ sidx,
+    kd_grad_rows_kernel(const float* __restrict__ zbuf, int V, __nv_bfloat16* __restrict__ gbuf,
+                        int g_row0, int c0, int c_cap, const int* __restrict__ rowmap, int s0,
+                        int s_rows, const int* __restrict__ nvalid, const int* __restrict__ sidx,
                         const float* __restrict__ sp, int K, const float* __restrict__ lse,
                         float grad_loss, float inv_tau, float c_log2) {
   const int lane = threadIdx.x & 31;
-  const int i = blockIdx.x * GRAD_WARPS + (threadIdx.x >> 5);
+  const int nseg = (V + GRAD_SEG - 1) / GRAD_SEG;
+  const int64_t wg = static_cast<int64_t>(blockIdx.x) * GRAD_WARPS + (threadIdx.x >> 5);
+  const int i = static_cast<int>(wg / nseg);         // row of the sub-chunk
+  const int v0 = static_cast<int>(wg - static_cast<int64_t>(i) * nseg) * GRAD_SEG;
+  const int v1 = min(V, v0 + GRAD_SEG);
   const int nv = *nvalid;
-  const int rows = max(0, min(nv - c0, cap));
-  float* z = zbuf + static_cast<int64_t>(i) * V;
-  uint4* g = reinterpret_cast<uint4*>(z);  // 8 bf16 per uint4
+  const int rows = max(0, min(nv - s0, s_rows));  // valid rows of the sub-chunk
+  const int cr = g_row0 + i;                       // row in the chunk's G buffer
+  uint4* g = reinterpret_cast<uint4*>(gbuf + static_cast<int64_t>(cr) * V);  // 8 bf16 each
   if (i >= rows) {  // whole warp
-    if (i < min(buf_rows, (rows + 63) & ~63))
-      for (int col = 8 * lane; col < V; col += 256) g[col >> 3] = make_uint4(0u, 0u, 0u, 0u);
+    const int cv = max(0, min(nv - c0, c_cap));    // valid rows of the chunk
+    if (cr >= cv && cr < min(c_cap, (cv + 63) & ~63))
+      for (int col = v0 + 8 * lane; col < v1; col += 256) g[col >> 3] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  const int64_t t = rowmap[c0 + i];
+  const float* z = zbuf + static_cast<int64_t>(i) * V;
+  const int64_t t = rowmap[s0 + i];
   const float sc = grad_loss / static_cast<float>(nv) * inv_tau;
   const float lb = lse[t] * LOG2E;
   const int* srow = sidx + t * K;
   const float* prow = sp + t * K;
-  int pos = 0;
-  int nxt = __ldg(srow);
-  for (int b0 = 0; b0 < V; b0 += GRAD_U * 256) {
+  int pos = lower_bound_row(srow, K, v0);
+  int nxt = pos < K ? __ldg(srow + pos) : INT_MAX;
+  for (int b0 = v0; b0 < v1; b0 += GRAD_U * 256) {
     float4 v[GRAD_U][2];
 #pragma unroll
     for (int u = 0; u < GRAD_U; ++u) {
@@ -1346,7 +1352,6 @@ __global__ void __launch_bounds__(32 * GRAD_WARPS)
         v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-    __syncwarp();  // every lane's loads of this block precede any write below
     float gg[GRAD_U][8];
 #pragma unroll
     for (int u = 0; u < GRAD_U; ++u) {

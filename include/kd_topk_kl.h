@@ -146,13 +146,15 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
  * chunk by chunk with memory bounded by one chunk): the same results, bit for
  * bit, as kd_topk_kl_forward followed by kd_topk_kl_backward with the same
  * arguments, in a single sweep that computes each row's logits once instead
- * of twice.  Rows are taken in the order valid rows, then invalid rows; per
- * chunk of `chunk` rows of that order the logit GEMM forms the lse partials
- * and the gather and also stores the chunk's fp32 logits (chunk x V x 4 bytes
- * of workspace, the only buffer whose size depends on V times a row count),
- * the chunk's lse and row_kl follow, a gradient pass turns the valid rows'
- * stored logits into the bf16 G in place, and the dh and dW contractions
- * consume it.  No T x V buffer exists at any time.
+ * of twice.  Rows are taken in the order valid rows, then invalid rows.  Per
+ * chunk of `chunk` rows of that order, and within it per half-chunk, the
+ * logit GEMM forms the lse partials and the gather and also stores the
+ * half-chunk's fp32 logits, the half-chunk's lse and row_kl follow, and a
+ * gradient pass turns its valid rows' stored logits into bf16 G in the
+ * chunk's G buffer; the chunk's dh and dW contractions then consume G.  The
+ * buffers whose size depends on V times a row count are the chunk's G
+ * (chunk x V x 2 bytes, as in kd_topk_kl_backward) and the half-chunk's
+ * logits (chunk/2 x V x 4 bytes).  No T x V buffer exists at any time.
  *
  * grad_loss: d(objective)/d(loss), as in kd_topk_kl_backward.
  * flags: 0 or KD_ACCUMULATE_DW.  With KD_ACCUMULATE_DW, dW += G^T h instead of
@@ -166,7 +168,7 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
  * Workspace bytes (*bytes) and number of kernel launches (*launches, the
  * status/counter resets and the dh zeroing are cudaMemsetAsync calls and are
  * not counted) of kd_topk_kl_forward_backward at this shape; either pointer
- * may be NULL.  About chunk * (4 V + 4 d) bytes plus O(T K) tables.
+ * may be NULL.  About 4 chunk V bytes plus O(T K + T V / 256) tables.
  * Host-only; KD_ERR_INVALID_ARG / KD_ERR_UNSUPPORTED on bad shapes.
  */
 int kd_topk_kl_forward_backward_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K,
