@@ -237,7 +237,8 @@ def workload_config(w, chunk):
 # ---------------------------------------------------------------- GPU run
 KERNEL_DESC = {
     "logits_fwd": "forward logit GEMM + online lse + gather",
-    "logits_fwd_sweep": "forward logit GEMM + online lse + gather + fp32 logit store (one chunk)",
+    "logits_fwd_sweep": "forward logit GEMM + online lse + gather + fp32 logit store, "
+                        "half a chunk of rows",
     "logits_bwd": "backward logit recompute + bf16 gradient tile",
     "dh": "dh^T = W^T G^T over the chunk's valid rows",
     "dW": "dW = G^T h_c, accumulated over chunks",
@@ -468,6 +469,9 @@ def run_ours(args, w, world, rank, local_rank):
         "config": dict(workload_config(w, chunk), parallelism=f"replicas x{world}"),
         "tflops_nominal": tf_nominal / world,
         "tflops_algorithmic": flops_alg / (ms_per_step / 1e3) / 1e12,
+        "flop_counts": ("nominal: the metric's 8 T d V (forward, recompute, dh, dW); "
+                        "algorithmic: the FLOPs performed, (2 T + 4 Nv) d V for the single sweep "
+                        "(no recompute) and (2 T + 6 Nv) d V for the split calls"),
         "frac_bf16_peak_burst": tf_nominal / world / burst,
         "frac_bf16_peak_sustained": tf_nominal / world / sustained,
         "api": "fused" if fused else "split", "variant": args.variant,
