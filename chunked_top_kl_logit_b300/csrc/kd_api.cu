@@ -148,7 +148,7 @@ Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk,
   L.fwd_total = off;
   L.rows_chunk = chunk < T ? chunk : T;
   L.dh_splits = dh_max_splits(V);
-  L.part_rows = L.dh_splits > 1 ? 2 * cdiv(L.rows_chunk, kGradBN) * kGradBN : 0;
+  L.part_rows = L.dh_splits > 1 ? (L.dh_splits - 1) * cdiv(L.rows_chunk, kGradBN) * kGradBN : 0;
   off = common;
   L.rowmap = off;     off += al256(static_cast<size_t>(T) * 4);
   L.split_info = off; off += 256;

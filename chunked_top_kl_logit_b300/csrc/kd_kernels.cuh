@@ -131,6 +131,9 @@ struct Sched {
   int m_tiles, n_tiles, num_tiles, k_steps, ks_per_split, splits, M, N;
 };
 
+// Longest contraction slab of a split dh (in BK steps): 51200 vocabulary columns.
+constexpr int DH_SLAB_STEPS = 800;
+
 // Split count for `tiles` output tiles over `k_steps` contraction steps: the
 // fewest splits whose (tile, split) units fill the policy's CTA count to 95%,
 // else the best fill; each split keeps at least 32 steps.
@@ -171,6 +174,10 @@ __device__ __forceinline__ Sched make_sched(const GemmParams& p) {
         int smax = p.splits;
         if (pad > 0) smax = min(smax, 1 + p.part_rows / pad);
         s.splits = pick_splits(s.m_tiles * s.n_tiles, s.k_steps, smax, p.policy_sms);
+        // a long contraction is also cut into slabs of at most DH_SLAB_STEPS steps:
+        // the split-major tile order then keeps the co-running CTAs on one slab of
+        // the operands, which stays in L2 (dh's DRAM re-reads fall)
+        s.splits = max(s.splits, min(smax, (s.k_steps + DH_SLAB_STEPS - 1) / DH_SLAB_STEPS));
         s.ks_per_split = (s.k_steps + s.splits - 1) / s.splits;
         if (p.split_info && blockIdx.x == 0 && threadIdx.x == 0) {
           p.split_info[0] = s.splits;
