@@ -118,19 +118,18 @@ struct Layout {
   size_t nvalid, losspart, sidx, sp, sslot, tterm, resid;  // shared by both passes
   size_t zg, part;                                  // forward
   size_t rowmap, split_info, hc, hct, dz, dhpart;   // backward
-  size_t szg, spart, srowkl, sz;                    // single sweep (sweep layouts only)
+  size_t szg, spart, srowkl, szmax;                 // single sweep (sweep layouts only)
   size_t fwd_total, bwd_total;
   int64_t rows_chunk;
-  int64_t rows_sub;   // single sweep: rows of a logit sub-chunk
   int dh_splits;      // largest split count of the dh contraction
   int64_t part_rows;  // rows of dh partials the split blocks may use
   int64_t hct_ld;     // row pitch (elements) of the transposed h chunk
 };
 
 // sweep: the single-sweep training step's layout: the backward's buffers (dz
-// holds the chunk's bf16 G), then the forward's tables for one sub-chunk and
-// the sub-chunk's fp32 logits (half a chunk, in whole 128-row tiles); bwd_total
-// is its size.
+// holds the chunk's G, and first the forward's relative logits), then the
+// forward's tables for one chunk and the largest logit of every (row, 32-column
+// chunk); bwd_total is its size.
 Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk,
                    bool sweep = false) {
   Layout L{};
@@ -158,12 +157,10 @@ Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk,
   L.dz = off;         off += al256(static_cast<size_t>(L.rows_chunk * V) * 2);
   L.dhpart = off;     off += al256(static_cast<size_t>(L.part_rows * d) * 4);
   if (sweep) {
-    L.rows_sub = cdiv(cdiv(L.rows_chunk, 2), BM) * BM;
-    if (L.rows_sub > L.rows_chunk) L.rows_sub = L.rows_chunk;
     L.szg = off;      off += al256(static_cast<size_t>(T * K) * 4);
-    L.spart = off;    off += al256(static_cast<size_t>(cdiv(V, ZBN) * L.rows_sub) * 4);
+    L.spart = off;    off += al256(static_cast<size_t>(cdiv(V, ZBN) * L.rows_chunk) * 4);
     L.srowkl = off;   off += al256(static_cast<size_t>(T) * 4);
-    L.sz = off;       off += al256(static_cast<size_t>(L.rows_sub * V) * 4);
+    L.szmax = off;    off += al256(static_cast<size_t>(L.rows_chunk * cdiv(V, 32)) * 4);
   }
   L.bwd_total = off;
   return L;
@@ -495,15 +492,10 @@ int kd_topk_kl_forward_backward_workspace_size(int64_t T, int64_t V, int64_t d, 
   if (rc != KD_OK) return rc;
   const Layout L = make_layout(T, V, d, K, chunk, true);
   if (bytes) *bytes = L.bwd_total;
-  // prep, row order; per sub-chunk: row gather, logit GEMM, combine, gradient
-  // pass; per chunk: transposed row gather, dh, [dh split reduce], dW; loss
-  // partials, loss
-  int64_t subs = 0;
-  for (int64_t c0 = 0; c0 < T; c0 += L.rows_chunk)
-    subs += cdiv((T - c0) < L.rows_chunk ? (T - c0) : L.rows_chunk, L.rows_sub);
+  // prep, row order; per chunk: row gather (plain and transposed), logit GEMM,
+  // combine, gradient pass, dh, [dh split reduce], dW; loss partials, loss
   if (launches)
-    *launches = static_cast<int32_t>(2 + subs * 4 +
-                                     cdiv(T, L.rows_chunk) * (L.dh_splits > 1 ? 4 : 3) + 2);
+    *launches = static_cast<int32_t>(2 + cdiv(T, L.rows_chunk) * (L.dh_splits > 1 ? 8 : 7) + 2);
   return KD_OK;
 }
 
@@ -739,14 +731,16 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
 
 // The single-sweep training step after the teacher prep (one logit GEMM per
 // row instead of two): rows in the order valid rows, then invalid rows.  Per
-// chunk of C rows of that order, and within it per sub-chunk of L.rows_sub
-// rows, the forward logit GEMM also stores the sub-chunk's fp32 logits, the
-// combine gives lse and row_kl of its rows, and the gradient pass turns its
-// valid rows' logits into bf16 G in the chunk's G buffer; the dh and dW
-// contractions of the chunk follow as in the backward.  The chunks of valid
-// rows are the backward's, and every value is formed by the same operations,
-// so the results equal forward + backward bit for bit (the loss too: its
-// partial sums are formed over the rows in their original order).
+// chunk of C rows of that order the forward logit GEMM forms the lse partials
+// and the gather and stores the valid rows' logits as fp16 values relative to
+// their 32-column chunk's largest (plus those largest logits) into the chunk's
+// G buffer, the combine gives lse and row_kl of the chunk's rows, a gradient
+// pass turns the stored values into bf16 G in place, and the dh and dW
+// contractions follow as in the backward.  The chunks of valid rows are the
+// backward's and the lse arithmetic is the forward's, so lse, row_kl and the
+// loss equal forward + backward bit for bit (the loss's partial sums are
+// formed over the rows in their original order); G, dh and dW agree to
+// within bf16 rounding.
 int enqueue_sweep(const void* h, const void* W, const uint8_t* valid, int64_t T, int64_t V,
                   int64_t d, int32_t K, float tau, const Layout& L, void* ws, const Ws& w,
                   int sms, float grad_loss, int accumulate_dW, float* loss,
@@ -762,11 +756,11 @@ int enqueue_sweep(const void* h, const void* W, const uint8_t* valid, int64_t T,
   float* dhpart = reinterpret_cast<float*>(wb + L.dhpart);
   float* zg = reinterpret_cast<float*>(wb + L.szg);
   float* part = reinterpret_cast<float*>(wb + L.spart);
-  float* zbuf = reinterpret_cast<float*>(wb + L.sz);
+  float* zmax = reinterpret_cast<float*>(wb + L.szmax);
   float* rkl = row_kl ? row_kl : reinterpret_cast<float*>(wb + L.srowkl);
   const float inv_tau = 1.0f / tau;
   const int64_t C = L.rows_chunk;
-  const int64_t S = L.rows_sub;
+  const int64_t nch = cdiv(V, 32);
 
   if (cudaMemsetAsync(dh, 0, static_cast<size_t>(T * d) * sizeof(float), st) != cudaSuccess)
     return KD_ERR_CUDA;
@@ -774,68 +768,66 @@ int enqueue_sweep(const void* h, const void* W, const uint8_t* valid, int64_t T,
   if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
 
   for (int64_t c0 = 0; c0 < T; c0 += C) {
-    const int64_t Mc = (T - c0) < C ? (T - c0) : C;
-    for (int64_t s0 = c0; s0 < c0 + Mc; s0 += S) {
-      const int64_t Ms = (c0 + Mc - s0) < S ? (c0 + Mc - s0) : S;
-      const bool last = s0 + Ms == c0 + Mc;
-      CUtensorMap ta, tb, tz;
-      // (0) the sub-chunk's rows of h in that order
-      kd_gather_rows_kernel<<<sms * 4, 256, 0, st>>>(
-          static_cast<const uint4*>(h), rowmap, nullptr, static_cast<int>(s0),
-          static_cast<int>(Ms), static_cast<int>(d / 8), reinterpret_cast<uint4*>(hc));
-      if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
-
-      // (1) logit tiles: lse partials, gather, fp32 logits stored
-      if (!make_map(&ta, hc, d, Ms, d, BM) || !make_map(&tb, W, d, V, d, ZBN) ||
-          !make_map_f32(&tz, zbuf, V, Ms, V, 32, 32, true))
-        return KD_ERR_CUDA;
-      GemmParams p = base_params(0, 0, ZBN);
-      logit_schedule(p, Ms, V, d);
-      p.status = dev_status;
-      p.K = K;
-      p.sidx = w.sidx;
-      p.sp = w.sp;
-      p.sslot = w.sslot;
-      p.inv_tau = inv_tau;
-      p.c_log2 = LOG2E * inv_tau;
-      p.part_ld = S;
-      p.part = part;
-      p.zg = zg;
-      p.gidx = nullptr;
-      p.nvalid = w.nvalid;
-      p.rowmap = rowmap;
-      p.rowmap_base = static_cast<int>(s0);
-      if ((rc = launch_gemm<EPI_FWDZ>(ta, tb, tz, ta, p, sms, st))) return rc;
-
-      // (2) lse and row_kl of the sub-chunk's rows
-      kd_combine_kernel<<<static_cast<unsigned>(cdiv(Ms, 32)), dim3(32, COMBINE_SPLIT), 0, st>>>(
-          part, S, p.n_tiles, static_cast<int>(Ms), K, rowmap, static_cast<int>(s0), w.sidx,
-          w.sp, zg, w.tterm, nullptr, valid, lse, rkl, nullptr, nullptr);
-      if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
-
-      // (3) G of its valid rows into the chunk's G buffer (the chunk's last
-      // sub-chunk also zeroes the rows after the chunk's valid ones)
-      const int64_t grid_rows = last ? C - (s0 - c0) : Ms;
-      const int slot = timing_slot(KD_KERNEL_GRAD_PASS);
-      if (slot >= 0 &&
-          cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
-        return KD_ERR_CUDA;
-      const int64_t warps = grid_rows * cdiv(V, GRAD_SEG);  // one per GRAD_SEG columns of a row
-      kd_grad_rows_kernel<<<static_cast<unsigned>(cdiv(warps, GRAD_WARPS)), 32 * GRAD_WARPS, 0,
-                            st>>>(zbuf, static_cast<int>(V), G, static_cast<int>(s0 - c0),
-                                     static_cast<int>(c0), static_cast<int>(C), rowmap,
-                                     static_cast<int>(s0), static_cast<int>(Ms), w.nvalid,
-                                     w.sidx, w.sp, K, lse, grad_loss, inv_tau, LOG2E * inv_tau);
-      if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
-      if (slot >= 0 &&
-          cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
-        return KD_ERR_CUDA;
-    }
-    // (4) dh and dW of the chunk
+    const int64_t M = (T - c0) < C ? (T - c0) : C;
+    CUtensorMap ta, tb, ty;
+    // (0) the chunk's rows of h in that order, and its valid rows transposed
+    kd_gather_rows_kernel<<<sms * 4, 256, 0, st>>>(
+        static_cast<const uint4*>(h), rowmap, nullptr, static_cast<int>(c0), static_cast<int>(M),
+        static_cast<int>(d / 8), reinterpret_cast<uint4*>(hc));
+    if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
     if ((rc = enqueue_gather_t(h, d, L, w, rowmap, c0, hct, st))) return rc;
-    if ((rc = enqueue_grad_contractions(W, V, d, L, w, sms, rowmap, G, V, hct, dhpart,
-                                        split_info, c0, dh, dW,
-                                        (c0 > 0 || accumulate_dW) ? 1 : 0, dev_status, st)))
+
+    // (1) logit tiles: lse partials, gather, the valid rows' relative logits
+    // into the G buffer (64-column x 32-row boxes of 16-bit values)
+    if (!make_map(&ta, hc, d, M, d, BM) || !make_map(&tb, W, d, V, d, ZBN) ||
+        !make_map(&ty, G, V, M, V, 32))
+      return KD_ERR_CUDA;
+    GemmParams p = base_params(0, 0, ZBN);
+    logit_schedule(p, M, V, d);
+    p.status = dev_status;
+    p.K = K;
+    p.sidx = w.sidx;
+    p.sp = w.sp;
+    p.sslot = w.sslot;
+    p.inv_tau = inv_tau;
+    p.c_log2 = LOG2E * inv_tau;
+    p.part_ld = C;
+    p.part = part;
+    p.zg = zg;
+    p.gidx = nullptr;
+    p.nvalid = w.nvalid;
+    p.rowmap = rowmap;
+    p.rowmap_base = static_cast<int>(c0);
+    p.zmax = zmax;
+    p.zmax_ld = nch;
+    if ((rc = launch_gemm<EPI_FWDZ>(ta, tb, ty, ta, p, sms, st))) return rc;
+
+    // (2) lse and row_kl of the chunk's rows
+    kd_combine_kernel<<<static_cast<unsigned>(cdiv(M, 32)), dim3(32, COMBINE_SPLIT), 0, st>>>(
+        part, C, p.n_tiles, static_cast<int>(M), K, rowmap, static_cast<int>(c0), w.sidx, w.sp,
+        zg, w.tterm, nullptr, valid, lse, rkl, nullptr, nullptr);
+    if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+
+    // (3) G of the chunk's valid rows, in place (the rows after them, up to the
+    // next multiple of 64, set to zero)
+    const int64_t warps = C * cdiv(V, GRAD_SEG);  // one per GRAD_SEG columns of a row
+    const int slot = timing_slot(KD_KERNEL_GRAD_PASS);
+    if (slot >= 0 &&
+        cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
+      return KD_ERR_CUDA;
+    kd_grad_rows_kernel<<<static_cast<unsigned>(cdiv(warps, GRAD_WARPS)), 32 * GRAD_WARPS, 0,
+                          st>>>(G, static_cast<int>(V), zmax, nch, static_cast<int>(c0),
+                                static_cast<int>(C), rowmap, w.nvalid, w.sidx, w.sp, K, lse,
+                                grad_loss, inv_tau, LOG2E * inv_tau);
+    if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
+    if (slot >= 0 &&
+        cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
+      return KD_ERR_CUDA;
+
+    // (4) dh and dW of the chunk
+    if ((rc = enqueue_grad_contractions(W, V, d, L, w, sms, rowmap, G, V, hct, dhpart, split_info,
+                                        c0, dh, dW, (c0 > 0 || accumulate_dW) ? 1 : 0,
+                                        dev_status, st)))
       return rc;
   }
   const int nb = static_cast<int>(cdiv(T, 32));

@@ -25,6 +25,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "kd_ptx.cuh"
@@ -124,6 +125,9 @@ struct GemmParams {
   // tile's largest logit goes to tkeys[row * n_tiles + tile]; the logits
   // themselves leave through the output tensor map (rows x vocabulary, fp32).
   uint64_t* tkeys;
+  // EPI_FWDZ: the largest raw logit of each (row, 32-column chunk), zmax[row * zmax_ld + chunk]
+  float* zmax;
+  int64_t zmax_ld;
 };
 
 // Per-launch schedule, resolved on the device at kernel start.
@@ -353,10 +357,15 @@ __device__ __forceinline__ uint32_t gather_chunk(const GemmParams& p, const uint
 // that the mass outside the cache is a sum of its own terms, never 1 minus
 // the cached mass.
 // STOREZ (single sweep): the launch covers rows rowmap[rowmap_base + local row]
-// of one chunk, valid rows first; the partial goes to part[tile][local row],
-// and warps holding valid rows also store the tile's fp32 logits through the
-// TMA (32 x 32 pieces staged in the 128-byte swizzle, as EPI_TMAX does) into
-// the chunk buffer that the gradient pass reads.
+// of one chunk, valid rows first; the partial goes to part[tile][local row].
+// Warps holding valid rows also store, for the gradient pass, every logit as
+// y = exp((z - zc) / tau) in fp16, relative to the largest raw logit zc of its
+// 32-column chunk (so y is in (0, 1] with the chunk's largest exactly 1), and
+// zc itself in zmax: y times exp(zc / tau - lse) is the student's q.  The y of
+// two chunks (32 rows x 64 columns, 128 bytes a row) are staged in the
+// 128-byte swizzle and the TMA stores the piece into the chunk's G buffer,
+// which the gradient pass then turns into G in place.  The lse arithmetic is
+// the plain forward's, so lse, row_kl and the loss equal it bit for bit.
 template <bool EXCL, bool STOREZ>
 __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, const TileCoord& c,
                                         int acc,
@@ -396,22 +405,39 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
     tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
     tmem_ld_wait(r);
     if (STOREZ && zstore) {  // warp-uniform
-      float* buf = stage_buf + (piece & 1u) * DW_PIECE_FLOATS;
-      if (lane == 0) bulk_wait_group_read<1>();  // the copy from this buffer two pieces ago is done
-      __syncwarp();
-      float4* b4 = reinterpret_cast<float4*>(buf);
+      float zc = -CUDART_INF_F;  // the chunk's largest raw logit inside the vocabulary
 #pragma unroll
-      for (int j = 0; j < 8; ++j)  // row `lane`, 16-byte chunk j, 128-byte swizzle
-        b4[lane * 8 + (j ^ (lane & 7))] =
-            make_float4(__uint_as_float(r[4 * j + 0]), __uint_as_float(r[4 * j + 1]),
-                        __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(tmC, buf, cb, lrow - lane);
-        bulk_commit_group();
+      for (int j = 0; j < 32; ++j) zc = cb + j < p.N ? fmaxf(zc, __uint_as_float(r[j])) : zc;
+      const float uzc = zc * p.c_log2;
+      uint32_t hy[16];  // y of the 32 columns as 16 pairs of fp16
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float y0 = cb + 2 * j < p.N ? ex2f(fmaf(__uint_as_float(r[2 * j]), p.c_log2, -uzc)) : 0.f;
+        const float y1 =
+            cb + 2 * j + 1 < p.N ? ex2f(fmaf(__uint_as_float(r[2 * j + 1]), p.c_log2, -uzc)) : 0.f;
+        const __half2 hh = __floats2half2_rn(y0, y1);
+        hy[j] = *reinterpret_cast<const uint32_t*>(&hh);
       }
-      ++piece;
+      if (row_ok) p.zmax[static_cast<int64_t>(lrow) * p.zmax_ld + (cb >> 5)] = zc;
+      const int hf = cc & 1;
+      uint4* b4 = reinterpret_cast<uint4*>(stage_buf + (piece & 1u) * DW_PIECE_FLOATS);
+      if (hf == 0) {  // a new 64-column piece: wait until its buffer is free
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)  // row `lane`, 16-byte chunk hf*4 + q, 128-byte swizzle
+        b4[lane * 8 + ((hf * 4 + q) ^ (lane & 7))] =
+            make_uint4(hy[4 * q + 0], hy[4 * q + 1], hy[4 * q + 2], hy[4 * q + 3]);
+      if (hf == 1 || cb + 32 >= p.N) {  // piece complete (or the vocabulary ends)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tmC, b4, cb - hf * 32, lrow - lane);
+          bulk_commit_group();
+        }
+        ++piece;
+      }
     }
     if (EXCL) {  // gather first, then sum the columns the gather did not hit
       const uint32_t hit = gather_chunk(p, r, cb, grow, srow, pos, nxt);
@@ -1294,91 +1320,87 @@ __global__ void kd_gather_rows_t_kernel(const __nv_bfloat16* __restrict__ h,
   }
 }
 
-// Gradient pass of the single sweep: G for the valid rows of one sub-chunk
-// (rowmap[s0 + i], i < its row count) from the fp32 logits the forward stored
-// (z row i, V floats), G = s (exp(z/tau - lse) - scatter p) / tau with
-// s = g / N_valid (every row here is valid), rounded to bf16 into row
-// g_row0 + i of the chunk's G buffer (V elements a row).  One warp per
-// GRAD_SEG columns of a row (so that a sub-chunk of a few thousand rows still
-// keeps every SM's memory pipes full), GRAD_U x 256 columns at a time, 8 per
-// lane.  The cached entries are walked
-// in ascending order and subtracted from the owning lane's value one slot at
-// a time, the same operations in the same order as the recompute epilogue
-// (EPI_DZ), each product and sum explicitly rounded (never contracted into an
-// FMA by the compiler, which could do so in one kernel and not the other), so
-// G is bit-identical to the split backward's.
-// Chunk rows from the chunk's valid count up to the next multiple of 64
-// (within the buffer's c_cap rows) get G = 0: the dW contraction reads whole
-// 64-row steps of G against zero rows of h_c^T, and stale bytes there could
-// hold NaN patterns, which 0 would not cancel.  Warps past the sub-chunk's
-// valid rows take those rows (the grid of a chunk's last sub-chunk reaches
-// c_cap).
+// Gradient pass of the single sweep, in place over the chunk's G buffer: row i
+// (i below the chunk's valid count; original row rowmap[c0 + i]) holds the
+// forward's y = exp((z - zc) / tau) in fp16 (zc = zmax[i][chunk], the largest
+// raw logit of the 32-column chunk), so q = y exp(zc / tau - lse) and
+// G = s (q - scatter p) with s = g / N_valid / tau; G replaces y as bf16.
+// A task is one warp on GRAD_SEG columns of a row (so that a chunk still keeps
+// every SM's memory pipes full), GRAD_U x 256 columns at a time, 8 per lane,
+// each lane reading and writing its own 16 bytes.  The cached entries are
+// walked in ascending order and subtracted from the owning lane's value one
+// slot at a time (a repeated index subtracts each slot's p).
+// Rows from the valid count up to the next multiple of 64 (within the
+// buffer's c_cap rows) get G = 0: the dW contraction reads whole 64-row steps
+// of G against zero rows of h_c^T, and the y left there (invalid rows' logits)
+// would otherwise add nonzero terms.
 constexpr int GRAD_WARPS = 8;
 constexpr int GRAD_U = 4;
-constexpr int GRAD_SEG = 16 * GRAD_U * 256;  // columns per warp
+constexpr int GRAD_SEG = 16 * GRAD_U * 256;  // columns per task
 
 __global__ void __launch_bounds__(32 * GRAD_WARPS)
-    kd_grad_rows_kernel(const float* __restrict__ zbuf, int V, __nv_bfloat16* __restrict__ gbuf,
-                        int g_row0, int c0, int c_cap, const int* __restrict__ rowmap, int s0,
-                        int s_rows, const int* __restrict__ nvalid, const int* __restrict__ sidx,
+    kd_grad_rows_kernel(__nv_bfloat16* __restrict__ gbuf, int V, const float* __restrict__ zmax,
+                        int64_t zmax_ld, int c0, int c_cap, const int* __restrict__ rowmap,
+                        const int* __restrict__ nvalid, const int* __restrict__ sidx,
                         const float* __restrict__ sp, int K, const float* __restrict__ lse,
                         float grad_loss, float inv_tau, float c_log2) {
   const int lane = threadIdx.x & 31;
   const int nseg = (V + GRAD_SEG - 1) / GRAD_SEG;
   const int64_t wg = static_cast<int64_t>(blockIdx.x) * GRAD_WARPS + (threadIdx.x >> 5);
-  const int i = static_cast<int>(wg / nseg);         // row of the sub-chunk
+  const int i = static_cast<int>(wg / nseg);  // row of the chunk
   const int v0 = static_cast<int>(wg - static_cast<int64_t>(i) * nseg) * GRAD_SEG;
   const int v1 = min(V, v0 + GRAD_SEG);
   const int nv = *nvalid;
-  const int rows = max(0, min(nv - s0, s_rows));  // valid rows of the sub-chunk
-  const int cr = g_row0 + i;                       // row in the chunk's G buffer
-  uint4* g = reinterpret_cast<uint4*>(gbuf + static_cast<int64_t>(cr) * V);  // 8 bf16 each
+  const int rows = max(0, min(nv - c0, c_cap));  // valid rows of the chunk
+  uint4* g = reinterpret_cast<uint4*>(gbuf + static_cast<int64_t>(i) * V);  // 8 elements each
   if (i >= rows) {  // whole warp
-    const int cv = max(0, min(nv - c0, c_cap));    // valid rows of the chunk
-    if (cr >= cv && cr < min(c_cap, (cv + 63) & ~63))
+    if (i < min(c_cap, (rows + 63) & ~63))
       for (int col = v0 + 8 * lane; col < v1; col += 256) g[col >> 3] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  const float* z = zbuf + static_cast<int64_t>(i) * V;
-  const int64_t t = rowmap[s0 + i];
+  const int64_t t = rowmap[c0 + i];
   const float sc = grad_loss / static_cast<float>(nv) * inv_tau;
   const float lb = lse[t] * LOG2E;
+  const float* zrow = zmax + static_cast<int64_t>(i) * zmax_ld;
   const int* srow = sidx + t * K;
   const float* prow = sp + t * K;
   int pos = lower_bound_row(srow, K, v0);
   int nxt = pos < K ? __ldg(srow + pos) : INT_MAX;
   for (int b0 = v0; b0 < v1; b0 += GRAD_U * 256) {
-    float4 v[GRAD_U][2];
+    uint4 v[GRAD_U];
+    float f[GRAD_U];
 #pragma unroll
     for (int u = 0; u < GRAD_U; ++u) {
       const int col = b0 + u * 256 + 8 * lane;
       if (col < V) {  // V % 8 == 0: a group is wholly inside or outside
-        v[u][0] = __ldcs(reinterpret_cast<const float4*>(z + col));
-        v[u][1] = __ldcs(reinterpret_cast<const float4*>(z + col) + 1);
+        v[u] = __ldcs(g + (col >> 3));
+        f[u] = sc * ex2f(fmaf(__ldg(zrow + (col >> 5)), c_log2, -lb));  // s exp(zc/tau - lse)
       } else {
-        v[u][0] = v[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        f[u] = 0.f;
       }
     }
     float gg[GRAD_U][8];
 #pragma unroll
     for (int u = 0; u < GRAD_U; ++u) {
-      const float zz[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
-                           v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+      const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        gg[u][j] = sc != 0.f ? __fmul_rn(sc, ex2f(fmaf(zz[j], c_log2, -lb))) : 0.f;
+      for (int j = 0; j < 4; ++j) {
+        const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&w4[j]));
+        gg[u][2 * j] = f[u] * y.x;
+        gg[u][2 * j + 1] = f[u] * y.y;
+      }
     }
     const int be = b0 + GRAD_U * 256;
     while (nxt < be) {  // warp-uniform: every lane walks the same row
       const int off = nxt - b0;
       const int uu = off >> 8, ln = (off >> 3) & 31, jj = off & 7;
-      const float add = -__fmul_rn(sc, __ldg(prow + pos));
+      const float add = -(sc * __ldg(prow + pos));
       if (lane == ln) {
 #pragma unroll
         for (int u = 0; u < GRAD_U; ++u)
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            gg[u][j] = (u == uu && j == jj) ? __fadd_rn(gg[u][j], add) : gg[u][j];
+          for (int j = 0; j < 8; ++j) gg[u][j] = (u == uu && j == jj) ? gg[u][j] + add : gg[u][j];
       }
       ++pos;
       nxt = pos < K ? __ldg(srow + pos) : INT_MAX;

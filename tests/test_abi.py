@@ -158,18 +158,19 @@ def test_forward_backward_argument_checks():
 
 
 def test_forward_backward_workspace_and_launch_count():
-    """The single sweep holds half a chunk of fp32 logits and the forward's
-    tables for it beside the backward's buffers (its bf16 G chunk included),
-    and makes 2 + half-chunks x 4 + chunks x (3 or 4) + 2 launches."""
+    """The single sweep needs the backward's buffers (its bf16 G chunk holds
+    the forward's relative logits first) plus the forward's tables for one
+    chunk and the largest logit of every (row, 32-column chunk), and makes
+    2 + chunks x (7 or 8) + 2 launches."""
     T, V, d, K = 32768, 201088, 2880, 100
     for chunk in (4096, 8192):
         f, b = kd.kd_topk_kl_workspace_size(T, V, d, K, chunk)
         sw, n = kd.kd_topk_kl_forward_backward_workspace_size(T, V, d, K, chunk)
         extra = sw - b
-        # + chunk/2 x V x 4 bytes of logits, + O(T K + V / 256 chunk / 2 + T)
-        assert chunk * V * 2 <= extra <= chunk * V * 2 + T * K * 4 + 786 * chunk * 2 + T * 4 + 4096
+        nch = -(-V // 32)
+        assert chunk * nch * 4 <= extra <= chunk * nch * 4 + T * K * 4 + 786 * chunk * 4 + T * 4 + 4096
         chunks = -(-T // chunk)
-        assert n in (2 + 2 * chunks * 4 + chunks * 3 + 2, 2 + 2 * chunks * 4 + chunks * 4 + 2)
+        assert n in (2 + chunks * 7 + 2, 2 + chunks * 8 + 2)
     with pytest.raises(kd.KDError):
         kd.kd_topk_kl_forward_backward_workspace_size(0, V, d, K, 64)
     with pytest.raises(kd.KDError):

@@ -11,7 +11,8 @@ lse and row_kl of every row; dh is compared on seeded rows and dW on seeded
 vocabulary rows, both computed by the oracle from its own lse; the gathered
 indices are compared in full.  Nothing the oracle uses comes from the GPU.
 At ctx_32k the one-call training step (the single sweep the benchmark times)
-must also equal the separate forward and backward bit for bit.
+must also give the separate calls' loss, lse and row_kl bit for bit, and dh
+and dW within the oracle's tolerance on the same sampled rows.
 
 The oracle's row blocks are larger here than its defaults only to make fewer,
 larger BLAS calls; a block is the plain definition applied to a set of rows.
@@ -117,13 +118,15 @@ def test_ctx_32k_full_forward_sampled_grads():
     gpu = run_gpu(x, w.chunk)
     assert_forward_parity(gpu, f)
     assert gpu["bwd_status"] == 0
-    sw = run_sweep(x, w.chunk)
-    assert sw["status"] == 0
-    for k in ("loss", "lse", "row_kl", "dh", "dW"):
-        np.testing.assert_array_equal(sw[k], gpu[k], err_msg=k)
-    del sw
     rows, vrows = _sampled_grads(w, gpu, P, f, seed=2, n_rows=512, n_vrows=640, slab=256)
     assert len(rows) >= 500 and len(vrows) >= 1024
+    sw = run_sweep(x, w.chunk)
+    assert sw["status"] == 0
+    for k in ("loss", "lse", "row_kl"):
+        np.testing.assert_array_equal(sw[k], gpu[k], err_msg=k)
+    _sampled_grads(w, sw, P, f, seed=2, n_rows=512, n_vrows=640, slab=256)
+    assert rel_l2(sw["dh"], gpu["dh"]) <= 2e-3 and rel_l2(sw["dW"], gpu["dW"]) <= 2e-3
+    del sw
     # every row of G sums to zero, so the column sums of dW vanish up to the
     # bf16 rounding of G (a property beside the oracle comparison above)
     col = gpu["dW"].sum(axis=0)
@@ -132,14 +135,15 @@ def test_ctx_32k_full_forward_sampled_grads():
 
 
 def test_ctx_32k_single_sweep_chunk_4096():
-    """The one-call training step at ctx_32k with 4096-row chunks: bit for bit
-    the separate forward and backward at the same chunk size, and held to the
-    oracle's full forward and its sampled gradients."""
+    """The one-call training step at ctx_32k with 4096-row chunks: loss, lse and
+    row_kl bit for bit those of the separate forward and backward at the same
+    chunk size, and held to the oracle's full forward and its sampled
+    gradients."""
     w, x, P, f = _inputs_and_forward("ctx_32k")
     sw = run_sweep(x, 4096)
     assert sw["status"] == 0
     gpu = run_gpu(x, 4096)
-    for k in ("loss", "lse", "row_kl", "dh", "dW"):
+    for k in ("loss", "lse", "row_kl"):
         np.testing.assert_array_equal(sw[k], gpu[k], err_msg=k)
     assert abs(sw["loss"] - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
     assert np.abs(sw["lse"] - f["lse"]).max() <= LSE_ATOL

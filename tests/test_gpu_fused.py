@@ -1,11 +1,14 @@
-"""The single-call training step kd_topk_kl_forward_backward, the dW
-accumulation flag and the loss-only forward, through the C ABI.
+"""The single-call training step kd_topk_kl_forward_backward (the single
+sweep), the dW accumulation flag and the loss-only forward, through the C ABI.
 
-The fused call runs the same kernels in the same order as the separate
-forward and backward, so its outputs must match them bit for bit; with
-KD_ACCUMULATE_DW, dW must equal the previous contents plus this batch's dW
-(fp32 rounding of the extra addition only); the loss-only forward (lse = NULL)
-must give the same loss.  One case is also held to the fp64 oracle."""
+The sweep forms each row's logits once: its lse arithmetic is the forward's,
+so loss, lse and row_kl must equal the separate forward and backward bit for
+bit; its G comes from fp16 logits relative to their 32-column chunk's
+largest, so dh and dW agree with the separate calls to within bf16 rounding
+(relative L2 <= SWEEP_RL2) and with the fp64 oracle to the project's
+tolerance.  With KD_ACCUMULATE_DW, dW must equal the previous contents plus
+this batch's dW (fp32 rounding of the extra addition only); the loss-only
+forward (lse = NULL) must give the same loss."""
 
 import numpy as np
 import pytest
@@ -17,6 +20,10 @@ from synth import make_inputs, workload
 from tests.gpu_util import GRAD_RL2, LOSS_RTOL, LSE_ATOL, oracle_inputs, rel_l2, to_device
 
 pytestmark = pytest.mark.gpu
+
+# relative L2 between the sweep's and the separate calls' dh and dW: both round
+# G to bf16 (2^-9), the sweep after a fp16 rounding of the relative logit
+SWEEP_RL2 = 2e-3
 
 CASES = [
     ("T600_V5000_d256_chunk200", dict(T=600, d=256, V=5000, K=50, tau=1.5), 200),
@@ -38,7 +45,7 @@ def _separate(g, chunk, grad_loss):
 
 
 @pytest.mark.parametrize("name,over,chunk", CASES, ids=[c[0] for c in CASES])
-def test_fused_equals_separate_bitwise(name, over, chunk):
+def test_fused_matches_separate(name, over, chunk):
     x = make_inputs(workload("small_4k", **over))
     g = to_device(x)
     a = _separate(g, chunk, 0.75)
@@ -49,8 +56,19 @@ def test_fused_equals_separate_bitwise(name, over, chunk):
                        0.75)
     torch.cuda.synchronize()
     kd.check_device_status(b.status, "fused")
-    for k in ("loss", "lse", "row_kl", "dh", "dW"):
+    for k in ("loss", "lse", "row_kl"):
         assert torch.equal(getattr(a, k), getattr(b, k)), k
+    for k in ("dh", "dW"):
+        assert rel_l2(getattr(b, k).double().cpu().numpy(),
+                      getattr(a, k).double().cpu().numpy()) <= SWEEP_RL2, k
+    assert bool((b.dh[g["valid"] == 0] == 0).all())
+    # and the oracle
+    P = oracle_inputs(x)
+    args = (P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], P["valid"], P["tau"])
+    f = O.forward(*args)
+    dh, dW = O.backward(*args, 0.75, lse=f["lse"])
+    assert rel_l2(b.dh.double().cpu().numpy(), dh) <= GRAD_RL2
+    assert rel_l2(b.dW.double().cpu().numpy(), dW) <= GRAD_RL2
 
 
 def test_fused_parity_with_oracle():
@@ -79,7 +97,9 @@ def test_accumulate_dW_adds_to_previous_contents(chunk):
     g = to_device(x)
     T, d = g["h"].shape
     V, K = g["W"].shape[0], g["teacher_idx"].shape[1]
-    ref = _separate(g, chunk, 1.0)
+    ref = kd.TopKKL(T, V, d, K, chunk)
+    ref.forward_backward(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"],
+                         g["tau"], 1.0)
     m = kd.TopKKL(T, V, d, K, chunk)
     prev = torch.randn(V, d, device="cuda", generator=torch.Generator("cuda").manual_seed(4))
     m.dW.copy_(prev)

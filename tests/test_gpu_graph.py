@@ -21,8 +21,11 @@ def test_step_replays_from_a_cuda_graph(fused):
     args = (g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"], g["tau"])
 
     eager = kd.TopKKL(T, V, d, K, 256)
-    eager.forward(*args)
-    eager.backward(*args, 1.0)
+    if fused:
+        eager.forward_backward(*args, 1.0)
+    else:
+        eager.forward(*args)
+        eager.backward(*args, 1.0)
     torch.cuda.synchronize()
     kd.check_device_status(eager.status, "eager")
 
