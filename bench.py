@@ -237,8 +237,8 @@ def workload_config(w, chunk):
 # ---------------------------------------------------------------- GPU run
 KERNEL_DESC = {
     "logits_fwd": "forward logit GEMM + online lse + gather",
-    "logits_fwd_sweep": "forward logit GEMM + online lse + gather + fp32 logit store, "
-                        "half a chunk of rows",
+    "logits_fwd_sweep": "forward logit GEMM + online lse + gather + fp16 relative logits "
+                        "stored into the chunk's G buffer",
     "logits_bwd": "backward logit recompute + bf16 gradient tile",
     "dh": "dh^T = W^T G^T over the chunk's valid rows",
     "dW": "dW = G^T h_c, accumulated over chunks",
@@ -249,8 +249,9 @@ def kernel_table(kstats: dict, steps: int, T: int, n_valid: int, d: int, V: int)
     """Per timed kernel: launches, time and achieved rate over the timed steps.
     Contractions (TFLOP/s), algorithmic FLOPs: 2 T d V for the forward logits,
     2 Nv d V for each backward contraction (masked rows are skipped).  The
-    single sweep's gradient pass (GB/s): 6 V bytes per valid row (its fp32
-    logits read, its bf16 G written)."""
+    single sweep's gradient pass (GB/s): 4.125 V bytes per valid row (its fp16
+    relative logits read and its bf16 G written in their place, one fp32
+    chunk maximum read per 32 columns)."""
     out = {}
     for name, (cnt, ms) in kstats.items():
         if cnt == 0:
@@ -258,7 +259,7 @@ def kernel_table(kstats: dict, steps: int, T: int, n_valid: int, d: int, V: int)
         row = {"launches": cnt, "ms_total": ms, "ms_per_step": ms / steps,
                "ms_per_launch": ms / cnt}
         if name == "grad_pass":
-            nbytes = 6.0 * n_valid * V * steps
+            nbytes = (4.0 + 4.0 / 32) * n_valid * V * steps
             row.update(bytes_per_launch=nbytes / cnt,
                        gbs=nbytes / (ms / 1e3) / 1e9 if ms > 0 else None)
         else:

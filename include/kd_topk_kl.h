@@ -143,18 +143,20 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
 /*
  * Forward and backward in one call, for a training step (the aipuls.nl
  * "Summary" describes the loss as the student's training objective, computed
- * chunk by chunk with memory bounded by one chunk): the same results, bit for
- * bit, as kd_topk_kl_forward followed by kd_topk_kl_backward with the same
- * arguments, in a single sweep that computes each row's logits once instead
- * of twice.  Rows are taken in the order valid rows, then invalid rows.  Per
- * chunk of `chunk` rows of that order, and within it per half-chunk, the
- * logit GEMM forms the lse partials and the gather and also stores the
- * half-chunk's fp32 logits, the half-chunk's lse and row_kl follow, and a
- * gradient pass turns its valid rows' stored logits into bf16 G in the
- * chunk's G buffer; the chunk's dh and dW contractions then consume G.  The
- * buffers whose size depends on V times a row count are the chunk's G
- * (chunk x V x 2 bytes, as in kd_topk_kl_backward) and the half-chunk's
- * logits (chunk/2 x V x 4 bytes).  No T x V buffer exists at any time.
+ * chunk by chunk with memory bounded by one chunk), in a single sweep that
+ * computes each row's logits once instead of twice.  Rows are taken in the
+ * order valid rows, then invalid rows; per chunk of `chunk` rows of that order
+ * the logit GEMM forms the lse partials and the gather and also stores every
+ * valid row's logits as fp16 values exp((z - zc) / tau) relative to the
+ * largest raw logit zc of their 32-column chunk (and those zc) into the
+ * chunk's G buffer (chunk x V x 2 bytes, as in kd_topk_kl_backward); the
+ * chunk's lse and row_kl follow, a gradient pass turns the stored values into
+ * bf16 G in place, and the chunk's dh and dW contractions consume it.  No
+ * T x V buffer exists at any time.
+ *
+ * Results: loss, lse and row_kl equal kd_topk_kl_forward's bit for bit; dh and
+ * dW equal kd_topk_kl_backward's to within bf16 rounding of G (the relative
+ * logit's fp16 rounding, 2^-11, comes before it).
  *
  * grad_loss: d(objective)/d(loss), as in kd_topk_kl_backward.
  * flags: 0 or KD_ACCUMULATE_DW.  With KD_ACCUMULATE_DW, dW += G^T h instead of
@@ -168,7 +170,8 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
  * Workspace bytes (*bytes) and number of kernel launches (*launches, the
  * status/counter resets and the dh zeroing are cudaMemsetAsync calls and are
  * not counted) of kd_topk_kl_forward_backward at this shape; either pointer
- * may be NULL.  About 4 chunk V bytes plus O(T K + T V / 256) tables.
+ * may be NULL.  About chunk * (2 V + V / 8) bytes plus O(T K) tables and the
+ * backward's chunk buffers.
  * Host-only; KD_ERR_INVALID_ARG / KD_ERR_UNSUPPORTED on bad shapes.
  */
 int kd_topk_kl_forward_backward_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K,
