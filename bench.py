@@ -156,15 +156,18 @@ def device_source_sha256() -> str:
     return h.hexdigest()
 
 
-def load_traffic(kernel: str):
+def load_traffic(kernel: str, workload: str, chunk: int):
     """DRAM bytes per launch of `kernel` from a committed ncu summary, only if
-    the device code still hashes to what was profiled (else None)."""
+    it was captured on this workload and chunk size and the device code still
+    hashes to what was profiled (else None)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f).get(kernel)
     if not d or d.get("device_sha256") != device_source_sha256():
+        return None
+    if d.get("workload") != workload or d.get("chunk") not in (None, chunk):
         return None
     return d.get("bytes_per_launch")
 
@@ -485,7 +488,8 @@ def run_ours(args, w, world, rank, local_rank):
                      "frac_of_burst": kd_dom["tflops"] / burst,
                      "flops_per_launch": kd_dom["flops_per_launch"],
                      "traffic": load_traffic("logits_fwd_sweep"
-                                             if (sweep and dom == "logits_fwd") else dom)},
+                                             if (sweep and dom == "logits_fwd") else dom,
+                                             w.name, chunk)},
         "memory": {"peak_allocated_bytes": int(peak),
                    "peak_minus_inputs_bytes": int(peak - base_alloc),
                    "device_free_drop_bytes": int(free_before - free_after),
@@ -573,9 +577,7 @@ def run_teacher_topk(args, w, world, rank, local_rank):
                      "peak": sustained, "unit": "TFLOP/s",
                      "frac": kern["topk_pass1"]["tflops"] / sustained,
                      "peak_kind": f"bf16 sustained, {src}",
-                     # measured at ctx_32k shapes with 4096-row chunks only
-                     "traffic": load_traffic("topk_pass1")
-                     if (w.name, chunk) == ("ctx_32k", 4096) else None},
+                     "traffic": load_traffic("topk_pass1", w.name, chunk)},
         "clocks": clocks,
         "gpu_launches": 4 * chunks * n,
     }
