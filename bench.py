@@ -240,29 +240,35 @@ def workload_config(w, chunk):
 # ---------------------------------------------------------------- GPU run
 KERNEL_DESC = {
     "logits_fwd": "forward logit GEMM + online lse + gather",
-    "logits_fwd_sweep": "forward logit GEMM + online lse + gather + fp16 relative logits "
-                        "stored into the chunk's G buffer",
+    "logits_fwd_sweep": "forward logit GEMM + online lse + gather + bf16 logits relative "
+                        "to the row offsets stored into the chunk's G buffer",
     "logits_bwd": "backward logit recompute + bf16 gradient tile",
     "dh": "dh^T = W^T G^T over the chunk's valid rows",
     "dW": "dW = G^T h_c, accumulated over chunks",
 }
 
 
-def kernel_table(kstats: dict, steps: int, T: int, n_valid: int, d: int, V: int) -> dict:
+def kernel_table(kstats: dict, steps: int, T: int, n_valid: int, d: int, V: int,
+                 K: int, sweep: bool = False) -> dict:
     """Per timed kernel: launches, time and achieved rate over the timed steps.
     Contractions (TFLOP/s), algorithmic FLOPs: 2 T d V for the forward logits,
     2 Nv d V for each backward contraction (masked rows are skipped).  The
-    single sweep's gradient pass (GB/s): 4.125 V bytes per valid row (its fp16
-    relative logits read and its bf16 G written in their place, one fp32
-    chunk maximum read per 32 columns)."""
+    single sweep's cached-column pass (GB/s): 14 K bytes per valid row (the
+    sorted index, the teacher probability and the gathered logit read, one
+    bf16 value written per slot); the zero rows it writes after a chunk's
+    valid rows are not counted.  In the single sweep the backward recompute
+    launch runs only for a chunk whose stored values would leave their range
+    (it returns at once otherwise), so it gets a time but no rate."""
     out = {}
     for name, (cnt, ms) in kstats.items():
         if cnt == 0:
             continue
         row = {"launches": cnt, "ms_total": ms, "ms_per_step": ms / steps,
                "ms_per_launch": ms / cnt}
-        if name == "grad_pass":
-            nbytes = (4.0 + 4.0 / 32) * n_valid * V * steps
+        if sweep and name == "logits_bwd":
+            row["note"] = "recompute of a flagged chunk's G (returns at once otherwise)"
+        elif name == "sweep_fix":
+            nbytes = 14.0 * K * n_valid * steps
             row.update(bytes_per_launch=nbytes / cnt,
                        gbs=nbytes / (ms / 1e3) / 1e9 if ms > 0 else None)
         else:
@@ -460,7 +466,7 @@ def run_ours(args, w, world, rank, local_rank):
     tf_nominal = flops_nominal / (ms_per_step / 1e3) / 1e12 * world
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    kernels = kernel_table(kstats, n, T, n_valid, d, V)
+    kernels = kernel_table(kstats, n, T, n_valid, d, V, K, sweep)
     contractions = [k for k, v in kernels.items() if "tflops" in v]
     dom = max(contractions, key=lambda k: kernels[k]["ms_per_step"])
     kd_dom = kernels[dom]

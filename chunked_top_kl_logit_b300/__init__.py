@@ -40,8 +40,8 @@ __all__ = [
 
 # contraction kernel ids of the diagnostic timing interface
 KERNELS = {"logits_fwd": 0, "logits_bwd": 1, "dh": 3, "dW": 4}
-# the single sweep's gradient pass (a SIMT kernel), timed the same way
-SWEEP_KERNELS = {"grad_pass": 7}
+# the single sweep's cached-column pass (a SIMT kernel), timed the same way
+SWEEP_KERNELS = {"sweep_fix": 7}
 PRODUCER_KERNELS = {"topk_pass1": 5, "topk_scan": 6}
 
 KD_OK = 0

@@ -118,7 +118,7 @@ struct Layout {
   size_t nvalid, losspart, sidx, sp, sslot, tterm, resid;  // shared by both passes
   size_t zg, part;                                  // forward
   size_t rowmap, split_info, hc, hct, dz, dhpart;   // backward
-  size_t szg, spart, srowkl, szmax;                 // single sweep (sweep layouts only)
+  size_t szg, spart, srowkl, sroff, srs, ses, sscal;  // single sweep (sweep layouts only)
   size_t fwd_total, bwd_total;
   int64_t rows_chunk;
   int dh_splits;      // largest split count of the dh contraction
@@ -127,9 +127,9 @@ struct Layout {
 };
 
 // sweep: the single-sweep training step's layout: the backward's buffers (dz
-// holds the chunk's G, and first the forward's relative logits), then the
-// forward's tables for one chunk and the largest logit of every (row, 32-column
-// chunk); bwd_total is its size.
+// holds the chunk's G, and first the forward's values relative to the row
+// offsets), then the forward's tables, the chunk's row offsets and scales, and
+// per chunk an overflow flag plus the dW factor; bwd_total is its size.
 Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk,
                    bool sweep = false) {
   Layout L{};
@@ -160,7 +160,10 @@ Layout make_layout(int64_t T, int64_t V, int64_t d, int64_t K, int64_t chunk,
     L.szg = off;      off += al256(static_cast<size_t>(T * K) * 4);
     L.spart = off;    off += al256(static_cast<size_t>(cdiv(V, ZBN) * L.rows_chunk) * 4);
     L.srowkl = off;   off += al256(static_cast<size_t>(T) * 4);
-    L.szmax = off;    off += al256(static_cast<size_t>(L.rows_chunk * cdiv(V, 32)) * 4);
+    L.sroff = off;    off += al256(static_cast<size_t>(L.rows_chunk) * 4);
+    L.srs = off;      off += al256(static_cast<size_t>(L.rows_chunk) * 4);
+    L.ses = off;      off += al256(static_cast<size_t>(L.rows_chunk) * 4);
+    L.sscal = off;    off += al256(static_cast<size_t>(cdiv(T, L.rows_chunk) + 1) * 4);
   }
   L.bwd_total = off;
   return L;
@@ -492,10 +495,11 @@ int kd_topk_kl_forward_backward_workspace_size(int64_t T, int64_t V, int64_t d, 
   if (rc != KD_OK) return rc;
   const Layout L = make_layout(T, V, d, K, chunk, true);
   if (bytes) *bytes = L.bwd_total;
-  // prep, row order; per chunk: row gather (plain and transposed), logit GEMM,
-  // combine, gradient pass, dh, [dh split reduce], dW; loss partials, loss
+  // prep, row order; per chunk: row gather with offsets, logit GEMM, combine,
+  // recompute (returns at once unless the chunk is flagged), cached columns,
+  // transposed row gather, dh, [dh split reduce], dW; loss partials, loss
   if (launches)
-    *launches = static_cast<int32_t>(2 + cdiv(T, L.rows_chunk) * (L.dh_splits > 1 ? 8 : 7) + 2);
+    *launches = static_cast<int32_t>(2 + cdiv(T, L.rows_chunk) * (L.dh_splits > 1 ? 9 : 8) + 2);
   return KD_OK;
 }
 
@@ -551,7 +555,8 @@ int enqueue_forward(const void* h, const void* W, const uint8_t* valid, int64_t 
   const int nb = static_cast<int>(cdiv(T, 32));
   kd_combine_kernel<<<nb, dim3(32, COMBINE_SPLIT), 0, st>>>(
       part, T, p.n_tiles, static_cast<int>(T), K, nullptr, 0, w.sidx, w.sp, zg, w.tterm,
-      var.residual() ? w.resid : nullptr, valid, lse, row_kl, var.outside_mass_out, w.losspart);
+      var.residual() ? w.resid : nullptr, valid, lse, row_kl, var.outside_mass_out, w.losspart,
+      SweepScales{});
   kd_loss_final_kernel<<<1, 256, 0, st>>>(w.losspart, nb, w.nvalid, loss);
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
@@ -565,7 +570,8 @@ int enqueue_grad_contractions(const void* W, int64_t V, int64_t d, const Layout&
                               int sms, const int* rowmap, const __nv_bfloat16* G, int64_t g_ld,
                               const __nv_bfloat16* hct, float* dhpart, int* split_info,
                               int64_t c0, float* dh, float* dW, int accumulate,
-                              int32_t* dev_status, cudaStream_t st) {
+                              const float* cscale, const float* oscale, int32_t* dev_status,
+                              cudaStream_t st) {
   int rc = KD_OK;
   const int S = L.dh_splits;
   const int64_t C = L.rows_chunk;
@@ -600,6 +606,7 @@ int enqueue_grad_contractions(const void* W, int64_t V, int64_t d, const Layout&
   q.part_rows = static_cast<int>(L.part_rows);
   q.policy_sms = kPolicySMs;
   q.split_info = split_info;
+  q.cscale = cscale;
   if ((rc = launch_gemm<EPI_DH>(ta, tb, ta, ta, q, sms, st))) return rc;
   if (S > 1) {
     kd_split_reduce_rows_kernel<<<sms * 4, 256, 0, st>>>(
@@ -637,20 +644,22 @@ int enqueue_grad_contractions(const void* W, int64_t V, int64_t d, const Layout&
   r.dyn_base = static_cast<int>(c0);
   r.dyn_cap = static_cast<int>(C);
   r.dyn_kind = 2;
+  r.oscale = oscale;
   return launch_gemm<EPI_DW>(ta, tb, tc, td, r, sms, st);
 }
 
 // The chunk's valid rows of h as h_c^T (dW's B operand): hcT[j][i] =
-// h[rowmap[c0 + i]][j] for the chunk's valid rows i, zero up to the pitch.
+// h[rowmap[c0 + i]][j] for the chunk's valid rows i (times escale[i] when
+// escale is not null), zero up to the pitch.
 int enqueue_gather_t(const void* h, int64_t d, const Layout& L, const Ws& w, const int* rowmap,
-                     int64_t c0, __nv_bfloat16* hct, cudaStream_t st) {
+                     int64_t c0, const float* escale, __nv_bfloat16* hct, cudaStream_t st) {
   const int64_t C = L.rows_chunk;
   kd_gather_rows_t_kernel<<<dim3(static_cast<unsigned>(cdiv(d, 32)),
                                  static_cast<unsigned>(cdiv(C, 32))),
                             dim3(32, 8), 0, st>>>(static_cast<const __nv_bfloat16*>(h), rowmap,
                                                   w.nvalid, static_cast<int>(c0),
                                                   static_cast<int>(C), static_cast<int>(L.hct_ld),
-                                                  static_cast<int>(d), hct);
+                                                  static_cast<int>(d), escale, hct);
   return cudaGetLastError() == cudaSuccess ? KD_OK : KD_ERR_CUDA;
 }
 
@@ -689,7 +698,7 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
         static_cast<const uint4*>(h), rowmap, w.nvalid, static_cast<int>(c0), static_cast<int>(C),
         static_cast<int>(d / 8), reinterpret_cast<uint4*>(hc));
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
-    if ((rc = enqueue_gather_t(h, d, L, w, rowmap, c0, hct, st))) return rc;
+    if ((rc = enqueue_gather_t(h, d, L, w, rowmap, c0, nullptr, hct, st))) return rc;
 
     // (1) recompute the chunk's logit tiles and write G as bf16
     if (!make_map(&ta, hc, d, C, d, BM) || !make_map(&tb, W, d, V, d, ZBN)) return KD_ERR_CUDA;
@@ -722,8 +731,8 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
 
     // (2), (3) dh and dW of the chunk
     if ((rc = enqueue_grad_contractions(W, V, d, L, w, sms, rowmap, dz, V, hct, dhpart, split_info,
-                                        c0, dh, dW, (c0 > 0 || accumulate_dW) ? 1 : 0,
-                                        dev_status, st)))
+                                        c0, dh, dW, (c0 > 0 || accumulate_dW) ? 1 : 0, nullptr,
+                                        nullptr, dev_status, st)))
       return rc;
   }
   return KD_OK;
@@ -731,17 +740,21 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
 
 // The single-sweep training step after the teacher prep (one logit GEMM per
 // row instead of two): rows in the order valid rows, then invalid rows.  Per
-// chunk of C rows of that order the forward logit GEMM forms the lse partials
-// and the gather and stores the valid rows' logits as fp16 values relative to
-// their 32-column chunk's largest (plus those largest logits) into the chunk's
-// G buffer, the combine gives lse and row_kl of the chunk's rows, a gradient
-// pass turns the stored values into bf16 G in place, and the dh and dW
-// contractions follow as in the backward.  The chunks of valid rows are the
-// backward's and the lse arithmetic is the forward's, so lse, row_kl and the
-// loss equal forward + backward bit for bit (the loss's partial sums are
-// formed over the rows in their original order); G, dh and dW agree to
-// within bf16 rounding.
-int enqueue_sweep(const void* h, const void* W, const uint8_t* valid, int64_t T, int64_t V,
+// chunk of C rows of that order: the rows of h and each valid row's offset o
+// (the student's logit at the teacher's highest cached entry); the forward
+// logit GEMM forms the lse partials and the gather and stores the valid rows'
+// logits as bf16 exp((z - o) / tau) into the chunk's G buffer; the combine
+// gives lse and row_kl and the scales exp(o / tau - lse); a chunk whose stored
+// values would have left their range has its G recomputed from the lse (a
+// launch that returns at once otherwise); the cached columns are corrected;
+// h_c^T is formed with the rows' scales, and the dh (scaled per row in its
+// epilogue) and dW contractions follow as in the backward.  The chunks of
+// valid rows are the backward's and the lse arithmetic is the forward's, so
+// lse, row_kl and the loss equal forward + backward bit for bit (the loss's
+// partial sums are formed over the rows in their original order); dh and dW
+// agree to within bf16 rounding.
+int enqueue_sweep(const void* h, const void* W, const int32_t* teacher_idx,
+                  const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
                   int64_t d, int32_t K, float tau, const Layout& L, void* ws, const Ws& w,
                   int sms, float grad_loss, int accumulate_dW, float* loss,
                   float* lse, float* row_kl, float* dh, float* dW, int32_t* dev_status,
@@ -756,29 +769,35 @@ int enqueue_sweep(const void* h, const void* W, const uint8_t* valid, int64_t T,
   float* dhpart = reinterpret_cast<float*>(wb + L.dhpart);
   float* zg = reinterpret_cast<float*>(wb + L.szg);
   float* part = reinterpret_cast<float*>(wb + L.spart);
-  float* zmax = reinterpret_cast<float*>(wb + L.szmax);
+  float* roff = reinterpret_cast<float*>(wb + L.sroff);
+  float* rscale = reinterpret_cast<float*>(wb + L.srs);
+  float* escale = reinterpret_cast<float*>(wb + L.ses);
+  float* oscale = reinterpret_cast<float*>(wb + L.sscal);  // then one flag per chunk
+  int* ovf = reinterpret_cast<int*>(oscale + 1);
   float* rkl = row_kl ? row_kl : reinterpret_cast<float*>(wb + L.srowkl);
   const float inv_tau = 1.0f / tau;
   const int64_t C = L.rows_chunk;
-  const int64_t nch = cdiv(V, 32);
+  const int64_t nchunks = cdiv(T, C);
 
-  if (cudaMemsetAsync(dh, 0, static_cast<size_t>(T * d) * sizeof(float), st) != cudaSuccess)
+  if (cudaMemsetAsync(dh, 0, static_cast<size_t>(T * d) * sizeof(float), st) != cudaSuccess ||
+      cudaMemsetAsync(ovf, 0, static_cast<size_t>(nchunks) * sizeof(int), st) != cudaSuccess)
     return KD_ERR_CUDA;
   kd_compact_rows_kernel<<<1, 1024, 0, st>>>(valid, static_cast<int>(T), w.nvalid, rowmap);
   if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
 
   for (int64_t c0 = 0; c0 < T; c0 += C) {
     const int64_t M = (T - c0) < C ? (T - c0) : C;
+    int* flag = ovf + c0 / C;
     CUtensorMap ta, tb, ty;
-    // (0) the chunk's rows of h in that order, and its valid rows transposed
-    kd_gather_rows_kernel<<<sms * 4, 256, 0, st>>>(
-        static_cast<const uint4*>(h), rowmap, nullptr, static_cast<int>(c0), static_cast<int>(M),
-        static_cast<int>(d / 8), reinterpret_cast<uint4*>(hc));
+    // (0) the chunk's rows of h in that order, and the valid rows' offsets
+    kd_gather_rows_offset_kernel<<<static_cast<unsigned>(cdiv(M, 8)), 256, 0, st>>>(
+        static_cast<const uint4*>(h), static_cast<const uint4*>(W), rowmap, w.nvalid, teacher_idx,
+        teacher_logits, K, static_cast<int>(V), static_cast<int>(c0), static_cast<int>(M),
+        static_cast<int>(d / 8), reinterpret_cast<uint4*>(hc), roff);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
-    if ((rc = enqueue_gather_t(h, d, L, w, rowmap, c0, hct, st))) return rc;
 
-    // (1) logit tiles: lse partials, gather, the valid rows' relative logits
-    // into the G buffer (64-column x 32-row boxes of 16-bit values)
+    // (1) logit tiles: lse partials, gather, the valid rows' values relative to
+    // their offsets into the G buffer (64-column x 32-row boxes of bf16)
     if (!make_map(&ta, hc, d, M, d, BM) || !make_map(&tb, W, d, V, d, ZBN) ||
         !make_map(&ty, G, V, M, V, 32))
       return KD_ERR_CUDA;
@@ -798,36 +817,61 @@ int enqueue_sweep(const void* h, const void* W, const uint8_t* valid, int64_t T,
     p.nvalid = w.nvalid;
     p.rowmap = rowmap;
     p.rowmap_base = static_cast<int>(c0);
-    p.zmax = zmax;
-    p.zmax_ld = nch;
+    p.roff = roff;
+    p.ovf = flag;
     if ((rc = launch_gemm<EPI_FWDZ>(ta, tb, ty, ta, p, sms, st))) return rc;
 
-    // (2) lse and row_kl of the chunk's rows
+    // (2) lse and row_kl of the chunk's rows, and the scales of the stored values
+    const SweepScales sc{roff, flag, w.nvalid, grad_loss, inv_tau, rscale, escale, oscale};
     kd_combine_kernel<<<static_cast<unsigned>(cdiv(M, 32)), dim3(32, COMBINE_SPLIT), 0, st>>>(
         part, C, p.n_tiles, static_cast<int>(M), K, rowmap, static_cast<int>(c0), w.sidx, w.sp,
-        zg, w.tterm, nullptr, valid, lse, rkl, nullptr, nullptr);
+        zg, w.tterm, nullptr, valid, lse, rkl, nullptr, nullptr, sc);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
 
-    // (3) G of the chunk's valid rows, in place (the rows after them, up to the
-    // next multiple of 64, set to zero)
-    const int64_t warps = C * cdiv(V, GRAD_SEG);  // one per GRAD_SEG columns of a row
-    const int slot = timing_slot(KD_KERNEL_GRAD_PASS);
+    // (3) only for a flagged chunk: G of its valid rows recomputed from the lse
+    GemmParams q = base_params(0, 0, ZBN);
+    logit_schedule(q, M, V, d);
+    q.status = dev_status;
+    q.K = K;
+    q.sidx = w.sidx;
+    q.sp = w.sp;
+    q.sslot = w.sslot;
+    q.inv_tau = inv_tau;
+    q.c_log2 = LOG2E * inv_tau;
+    q.lse = lse;
+    q.valid = valid;
+    q.nvalid = w.nvalid;
+    q.grad_loss = grad_loss;
+    q.dz = G;
+    q.dz_ld = V;
+    q.dyn_count = w.nvalid;
+    q.dyn_base = static_cast<int>(c0);
+    q.dyn_cap = static_cast<int>(M);
+    q.dyn_kind = 1;
+    q.rowmap = rowmap;
+    q.rowmap_base = static_cast<int>(c0);
+    q.gate = flag;
+    if ((rc = launch_gemm<EPI_DZ>(ta, tb, ty, ta, q, sms, st))) return rc;
+
+    // (4) the cached columns (and zero rows after the valid ones, up to the next
+    // multiple of 64)
+    const int slot = timing_slot(KD_KERNEL_SWEEP_FIX);
     if (slot >= 0 &&
         cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
       return KD_ERR_CUDA;
-    kd_grad_rows_kernel<<<static_cast<unsigned>(cdiv(warps, GRAD_WARPS)), 32 * GRAD_WARPS, 0,
-                          st>>>(G, static_cast<int>(V), zmax, nch, static_cast<int>(c0),
-                                static_cast<int>(C), rowmap, w.nvalid, w.sidx, w.sp, K, lse,
-                                grad_loss, inv_tau, LOG2E * inv_tau);
+    kd_fix_cached_kernel<<<static_cast<unsigned>(cdiv(C, FIX_WARPS)), 32 * FIX_WARPS, 0, st>>>(
+        G, static_cast<int>(V), static_cast<int>(c0), static_cast<int>(C), rowmap, w.nvalid, w.sidx,
+        w.sp, zg, K, lse, roff, inv_tau, flag);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
     if (slot >= 0 &&
         cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
       return KD_ERR_CUDA;
 
-    // (4) dh and dW of the chunk
+    // (5) h_c^T with the rows' scales, then dh and dW of the chunk
+    if ((rc = enqueue_gather_t(h, d, L, w, rowmap, c0, escale, hct, st))) return rc;
     if ((rc = enqueue_grad_contractions(W, V, d, L, w, sms, rowmap, G, V, hct, dhpart, split_info,
-                                        c0, dh, dW, (c0 > 0 || accumulate_dW) ? 1 : 0,
-                                        dev_status, st)))
+                                        c0, dh, dW, (c0 > 0 || accumulate_dW) ? 1 : 0, rscale,
+                                        oscale, dev_status, st)))
       return rc;
   }
   const int nb = static_cast<int>(cdiv(T, 32));
@@ -913,9 +957,9 @@ int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* tea
   if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
                      st)))
     return rc;
-  return enqueue_sweep(h, W, valid, T, V, d, K, tau, L, ws, w, sms, grad_loss,
-                       (flags & KD_ACCUMULATE_DW) ? 1 : 0, loss, lse, row_kl, dh, dW, dev_status,
-                       st);
+  return enqueue_sweep(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, L, ws, w, sms,
+                       grad_loss, (flags & KD_ACCUMULATE_DW) ? 1 : 0, loss, lse, row_kl, dh, dW,
+                       dev_status, st);
 }
 
 int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t Kd,

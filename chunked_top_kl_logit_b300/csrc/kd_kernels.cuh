@@ -25,7 +25,6 @@
 #pragma once
 
 #include <cuda_bf16.h>
-#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "kd_ptx.cuh"
@@ -125,10 +124,25 @@ struct GemmParams {
   // tile's largest logit goes to tkeys[row * n_tiles + tile]; the logits
   // themselves leave through the output tensor map (rows x vocabulary, fp32).
   uint64_t* tkeys;
-  // EPI_FWDZ: the largest raw logit of each (row, 32-column chunk), zmax[row * zmax_ld + chunk]
-  float* zmax;
-  int64_t zmax_ld;
+  // EPI_FWDZ (single sweep): the offset o of each local row (a raw logit) that
+  // the stored values exp((z - o) / tau) are relative to, and the chunk's
+  // flag, set when a stored value would leave the range that the later steps
+  // can take (the chunk's G is then recomputed from the known lse).
+  const float* roff;
+  int* ovf;
+  // EPI_DH: per-column (local chunk row) factor applied to the stored tile, or
+  // null.  EPI_DW: device scalar factor applied to the stored tile, or null.
+  const float* cscale;
+  const float* oscale;
+  // Launch gate: with gate != null the whole launch returns at once unless
+  // *gate != 0 (set on the device by an earlier kernel of the stream).
+  const int* gate;
 };
+
+// Largest c (zc - o) (log2 units) that a stored value may reach before the
+// chunk is flagged for recompute: 2^64 keeps the values, the sums of the dh
+// contraction and the scales exp(o / tau - lse) inside fp32 / bf16 range.
+constexpr float YREL_MAX_LOG2 = 64.f;
 
 // Per-launch schedule, resolved on the device at kernel start.
 struct Sched {
@@ -358,14 +372,20 @@ __device__ __forceinline__ uint32_t gather_chunk(const GemmParams& p, const uint
 // the cached mass.
 // STOREZ (single sweep): the launch covers rows rowmap[rowmap_base + local row]
 // of one chunk, valid rows first; the partial goes to part[tile][local row].
-// Warps holding valid rows also store, for the gradient pass, every logit as
-// y = exp((z - zc) / tau) in fp16, relative to the largest raw logit zc of its
-// 32-column chunk (so y is in (0, 1] with the chunk's largest exactly 1), and
-// zc itself in zmax: y times exp(zc / tau - lse) is the student's q.  The y of
-// two chunks (32 rows x 64 columns, 128 bytes a row) are staged in the
-// 128-byte swizzle and the TMA stores the piece into the chunk's G buffer,
-// which the gradient pass then turns into G in place.  The lse arithmetic is
-// the plain forward's, so lse, row_kl and the loss equal it bit for bit.
+// Warps holding valid rows also store, for the contractions that follow, each
+// valid row's logits as bf16 values exp((z - o) / tau) relative to the row's
+// offset o (roff[local row], a logit of the row, so that the largest value is
+// at least about 1); other rows of those warps store 0.  Formed as y times
+// 2^(c zc - c o) from the chunk-relative y of the lse sum, so one exponential
+// per element serves both.  G of the row is then rscale times these values
+// once the cached columns are corrected: the dh contraction applies the scale
+// to its output columns and the dW contraction takes it inside h_c^T.  A row
+// whose largest logit lies more than YREL_MAX_LOG2 / c above o flags the chunk
+// (ovf), whose G is then recomputed from the lse.  The values of two 32-column
+// chunks (32 rows x 64 columns, 128 bytes a row) are staged in the 128-byte
+// swizzle and the TMA stores the piece into the chunk's G buffer.  The lse
+// arithmetic is the plain forward's, so lse, row_kl and the loss equal it bit
+// for bit.
 template <bool EXCL, bool STOREZ>
 __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, const TileCoord& c,
                                         int acc,
@@ -378,10 +398,14 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
   const bool row_ok = lrow < sc_.M;
   int64_t grow = static_cast<int64_t>(p.row0) + lrow;
   bool zstore = false;
+  bool yrow = false;  // STOREZ: a valid row, whose values are stored
+  float uo = 0.f;     // STOREZ: c o, the row's offset in log2 units
   if (STOREZ) {
     grow = row_ok ? p.rowmap[p.rowmap_base + lrow] : 0;
     const int nvc = min(max(*p.nvalid - p.rowmap_base, 0), sc_.M);
     zstore = lrow - lane < nvc;  // warp-uniform: the warp's first row is valid
+    yrow = lrow < nvc;
+    if (yrow) uo = __fmul_rn(p.roff[lrow], p.c_log2);
   }
   const int v0 = c.n * ZBN;
   const int* srow = p.sidx + grow * p.K;
@@ -404,41 +428,6 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
     uint32_t r[32];
     tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
     tmem_ld_wait(r);
-    if (STOREZ && zstore) {  // warp-uniform
-      float zc = -CUDART_INF_F;  // the chunk's largest raw logit inside the vocabulary
-#pragma unroll
-      for (int j = 0; j < 32; ++j) zc = cb + j < p.N ? fmaxf(zc, __uint_as_float(r[j])) : zc;
-      const float uzc = zc * p.c_log2;
-      uint32_t hy[16];  // y of the 32 columns as 16 pairs of fp16
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float y0 = cb + 2 * j < p.N ? ex2f(fmaf(__uint_as_float(r[2 * j]), p.c_log2, -uzc)) : 0.f;
-        const float y1 =
-            cb + 2 * j + 1 < p.N ? ex2f(fmaf(__uint_as_float(r[2 * j + 1]), p.c_log2, -uzc)) : 0.f;
-        const __half2 hh = __floats2half2_rn(y0, y1);
-        hy[j] = *reinterpret_cast<const uint32_t*>(&hh);
-      }
-      if (row_ok) p.zmax[static_cast<int64_t>(lrow) * p.zmax_ld + (cb >> 5)] = zc;
-      const int hf = cc & 1;
-      uint4* b4 = reinterpret_cast<uint4*>(stage_buf + (piece & 1u) * DW_PIECE_FLOATS);
-      if (hf == 0) {  // a new 64-column piece: wait until its buffer is free
-        if (lane == 0) bulk_wait_group_read<1>();
-        __syncwarp();
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)  // row `lane`, 16-byte chunk hf*4 + q, 128-byte swizzle
-        b4[lane * 8 + ((hf * 4 + q) ^ (lane & 7))] =
-            make_uint4(hy[4 * q + 0], hy[4 * q + 1], hy[4 * q + 2], hy[4 * q + 3]);
-      if (hf == 1 || cb + 32 >= p.N) {  // piece complete (or the vocabulary ends)
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          tma_store_2d(tmC, b4, cb - hf * 32, lrow - lane);
-          bulk_commit_group();
-        }
-        ++piece;
-      }
-    }
     if (EXCL) {  // gather first, then sum the columns the gather did not hit
       const uint32_t hit = gather_chunk(p, r, cb, grow, srow, pos, nxt);
       float u[32];
@@ -459,30 +448,61 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
       }
       continue;
     }
+    // The chunk's largest raw logit zc inside the vocabulary (c > 0, so c zc is
+    // the largest scaled one), then y_j = 2^(c z_j - c zc) in (0, 1]: one FFMA
+    // and one ex2 per element give the lse term and, in the single sweep, the
+    // stored relative logit.  The rounding is pinned (explicit _rn operations),
+    // so that the sweep's lse equals the plain forward's bit for bit.
+    const bool full = cb + 32 <= p.N;  // uniform: all 32 columns inside the vocabulary
+    float zc = -CUDART_INF_F;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      zc = (full || cb + j < p.N) ? fmaxf(zc, __uint_as_float(r[j])) : zc;
+    const float uzc = __fmul_rn(zc, p.c_log2);
+    float f = 0.f;  // STOREZ: 2^(c zc - c o), from y to the stored value (0: a row not stored)
+    if (STOREZ && yrow) {
+      const float e = uzc - uo;
+      if (e > YREL_MAX_LOG2) *p.ovf = 1;  // the chunk's G is recomputed instead
+      f = ex2f(e);
+    }
     float cs = 0.f;
-    if (cb + 32 <= p.N) {  // uniform: all 32 columns inside the vocabulary
-      // max on the raw logits (c > 0), then one FFMA + one ex2 per element
-      float cz = __uint_as_float(r[0]);
+    uint32_t hy[16];  // STOREZ: the 32 stored values as 16 pairs of bf16
 #pragma unroll
-      for (int j = 1; j < 32; ++j) cz = fmaxf(cz, __uint_as_float(r[j]));
-      const float mn = fmaxf(m, cz * p.c_log2);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) cs += ex2f(fmaf(__uint_as_float(r[j]), p.c_log2, -mn));
-      s = s * ex2f(m - mn) + cs;
-      m = mn;
-    } else {  // the vocabulary ends inside this chunk
-      float u[32];
-      float cm = -CUDART_INF_F;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        u[j] = (cb + j < p.N) ? __uint_as_float(r[j]) * p.c_log2 : -CUDART_INF_F;
-        cm = fmaxf(cm, u[j]);
+    for (int j = 0; j < 16; ++j) {
+      const float y0 =
+          (full || cb + 2 * j < p.N) ? ex2f(fmaf(__uint_as_float(r[2 * j]), p.c_log2, -uzc)) : 0.f;
+      const float y1 = (full || cb + 2 * j + 1 < p.N)
+                           ? ex2f(fmaf(__uint_as_float(r[2 * j + 1]), p.c_log2, -uzc))
+                           : 0.f;
+      cs = __fadd_rn(__fadd_rn(cs, y0), y1);
+      if (STOREZ) {
+        const __nv_bfloat162 hb = __floats2bfloat162_rn(__fmul_rn(y0, f), __fmul_rn(y1, f));
+        hy[j] = *reinterpret_cast<const uint32_t*>(&hb);
       }
-      const float mn = fmaxf(m, cm);
+    }
+    const float mn = fmaxf(m, uzc);
+    s = __fadd_rn(__fmul_rn(s, ex2f(m - mn)), __fmul_rn(cs, ex2f(uzc - mn)));
+    m = mn;
+    if (STOREZ && zstore) {  // warp-uniform
+      const int hf = cc & 1;
+      uint4* b4 = reinterpret_cast<uint4*>(stage_buf + (piece & 1u) * DW_PIECE_FLOATS);
+      if (hf == 0) {  // a new 64-column piece: wait until its buffer is free
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+      }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) cs += ex2f(u[j] - mn);
-      s = s * ex2f(m - mn) + cs;
-      m = mn;
+      for (int q = 0; q < 4; ++q)  // row `lane`, 16-byte chunk hf*4 + q, 128-byte swizzle
+        b4[lane * 8 + ((hf * 4 + q) ^ (lane & 7))] =
+            make_uint4(hy[4 * q + 0], hy[4 * q + 1], hy[4 * q + 2], hy[4 * q + 3]);
+      if (hf == 1 || cb + 32 >= p.N) {  // piece complete (or the vocabulary ends)
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(tmC, b4, cb - hf * 32, lrow - lane);
+          bulk_commit_group();
+        }
+        ++piece;
+      }
     }
     gather_chunk(p, r, cb, grow, srow, pos, nxt);
   }
@@ -672,6 +692,7 @@ __device__ __forceinline__ void epi_store(const GemmParams& p, const Sched& sc_,
 //           original row rowmap[rowmap_base + n], split s >= 1 writes its
 //           partial block out2 + (s-1) * (n_tiles*BN) * ld_out at row n.
 //   EPI_DW: n is a vocabulary row; accumulate adds into the existing dW.
+// cscale != null: column n of the tile is multiplied by cscale[n] first.
 __device__ __forceinline__ void epi_store_t(const GemmParams& p, const Sched& sc_,
                                             const TileCoord& c, int acc, uint32_t tmem_row,
                                             int r_in_tile, uint64_t* tfull, uint64_t* tempty,
@@ -710,6 +731,12 @@ __device__ __forceinline__ void epi_store_t(const GemmParams& p, const Sched& sc
     int orow[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) orow[j] = __shfl_sync(0xffffffffu, my_row, j);
+    if (p.cscale) {  // uniform: the column's factor (a chunk row's G scale)
+      const float my_sc = cb + lane < sc_.N ? p.cscale[cb + lane] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        r[j] = __float_as_uint(__uint_as_float(r[j]) * __shfl_sync(0xffffffffu, my_sc, j));
+    }
     const int ncols = min(32, sc_.N - cb);
     if (m_ok) {
       float o[32];
@@ -736,7 +763,8 @@ __device__ __forceinline__ void epi_store_t(const GemmParams& p, const Sched& sc
 // ends with a 16-column piece, staged unswizzled for its own tensor map (tmD).
 // Each output element has exactly one owner per launch, so the sum is
 // deterministic.  No barrier spans warps, so a warp that leaves early on an
-// abort cannot leave another waiting.
+// abort cannot leave another waiting.  oscale != null: the tile is multiplied
+// by *oscale first.
 __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, const TileCoord& c,
                                        int acc, uint32_t tmem_row, int q, uint64_t* tfull,
                                        uint64_t* tempty, uint32_t use, volatile int* abort_flag,
@@ -748,6 +776,7 @@ __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, co
   const int n0 = c.n * p.BN;
   const bool accum = p.accumulate != 0;
   const bool kempty = sc_.k_steps == 0;   // no valid row in this chunk
+  const float osc = p.oscale ? *p.oscale : 1.f;
   bool w = mbar_wait(&tfull[acc], use & 1u, abort_flag, p.status);
   ok = __all_sync(0xffffffffu, w);
   if (!ok) return;
@@ -765,6 +794,10 @@ __device__ __forceinline__ void epi_dw(const GemmParams& p, const Sched& sc_, co
     } else {
       tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
       tmem_ld_wait(r);
+      if (p.oscale) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * osc);
+      }
     }
     float* buf = stage_buf + (piece & 1u) * DW_PIECE_FLOATS;
     if (lane == 0) bulk_wait_group_read<1>();  // the copy from this buffer two pieces ago is done
@@ -886,6 +919,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                    const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmC,
                    const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+  if (p.gate != nullptr && *p.gate == 0) return;  // uniform: nothing to do in this launch
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -1094,6 +1128,22 @@ __device__ __forceinline__ float merge_lse(const float (&sm)[COMBINE_SPLIT][32],
   return M + logf(S);
 }
 
+// The single sweep's scales of the chunk's stored values, formed with the lse
+// (rscale == null everywhere else).  For local row i below the chunk's valid
+// count: escale[i] = exp(o_i / tau - lse) and rscale[i] = s escale[i], with
+// s = grad_loss / N_valid / tau, so that G = rscale times the stored values;
+// *oscale = s.  When the chunk is flagged (ovf), its G is recomputed whole and
+// the scales are 1.  Rows past the valid count get 0.
+struct SweepScales {
+  const float* roff;
+  const int* ovf;
+  const int* nvalid;
+  float grad_loss, inv_tau;
+  float* rscale;
+  float* escale;
+  float* oscale;
+};
+
 __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
     kd_combine_kernel(const float* __restrict__ part, int64_t part_ld, int n_tiles, int T, int K,
                       const int* __restrict__ rowmap, int rowmap_base,
@@ -1101,7 +1151,8 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
                       const float* __restrict__ zg, const float* __restrict__ tterm,
                       const float* __restrict__ resid, const uint8_t* __restrict__ valid,
                       float* __restrict__ lse_out, float* __restrict__ row_kl_out,
-                      float* __restrict__ outside_mass_out, double* __restrict__ losspart) {
+                      float* __restrict__ outside_mass_out, double* __restrict__ losspart,
+                      const SweepScales sw) {
   __shared__ float sm[COMBINE_SPLIT][32], ss[COMBINE_SPLIT][32];
   __shared__ float s_lse[32], s_lu[32];
   __shared__ float sa[COMBINE_SPLIT][32], smass[COMBINE_SPLIT][32];
@@ -1124,6 +1175,21 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
     const float L = merge_lse(sm, ss, x);
     s_lse[x] = L;
     if (in && lse_out && !resid) lse_out[row] = L;
+    if (sw.rscale) {  // uniform
+      const int nv = *sw.nvalid;
+      const bool redo = *sw.ovf != 0;
+      const float sg = nv > 0 ? sw.grad_loss / static_cast<float>(nv) * sw.inv_tau : 0.f;
+      if (in) {
+        float e = 0.f, c = 0.f;
+        if (li < nv - rowmap_base) {
+          e = redo ? 1.f : expf(sw.roff[li] * sw.inv_tau - L);
+          c = redo ? 1.f : sg * e;
+        }
+        sw.escale[li] = e;
+        sw.rscale[li] = c;
+      }
+      if (blockIdx.x == 0 && x == 0) *sw.oscale = redo ? 1.f : sg;
+    }
   }
   __syncthreads();
   if (resid) {  // uniform: the cached columns complete the normaliser
@@ -1293,11 +1359,13 @@ __global__ void kd_gather_rows_kernel(const uint4* __restrict__ h, const int* __
 
 // The chunk's valid rows of h, transposed: hcT[j * ld + i] = h[rowmap[c0 + i]][j]
 // for i < rows and 0 for rows <= i < cap, rows = clamp(*nvalid - c0, 0, cap).
-// 32 x 32 tiles through shared memory; block (32, 8).
+// escale != null (single sweep): row i is multiplied by escale[i] and rounded
+// to bf16.  32 x 32 tiles through shared memory; block (32, 8).
 __global__ void kd_gather_rows_t_kernel(const __nv_bfloat16* __restrict__ h,
                                         const int* __restrict__ rowmap,
                                         const int* __restrict__ nvalid, int c0, int cap, int ld,
-                                        int d, __nv_bfloat16* __restrict__ hcT) {
+                                        int d, const float* __restrict__ escale,
+                                        __nv_bfloat16* __restrict__ hcT) {
   __shared__ __nv_bfloat16 tile[32][33];
   const int rows = max(0, min(*nvalid - c0, cap));
   const int j0 = blockIdx.x * 32;
@@ -1308,7 +1376,10 @@ __global__ void kd_gather_rows_t_kernel(const __nv_bfloat16* __restrict__ h,
     const int i = i0 + ty + 8 * r;
     const int j = j0 + tx;
     __nv_bfloat16 v = __float2bfloat16_rn(0.f);
-    if (i < rows && j < d) v = h[static_cast<int64_t>(rowmap[c0 + i]) * d + j];
+    if (i < rows && j < d) {
+      v = h[static_cast<int64_t>(rowmap[c0 + i]) * d + j];
+      if (escale) v = __float2bfloat16_rn(__bfloat162float(v) * escale[i]);
+    }
     tile[ty + 8 * r][tx] = v;
   }
   __syncthreads();
@@ -1320,106 +1391,115 @@ __global__ void kd_gather_rows_t_kernel(const __nv_bfloat16* __restrict__ h,
   }
 }
 
-// Gradient pass of the single sweep, in place over the chunk's G buffer: row i
-// (i below the chunk's valid count; original row rowmap[c0 + i]) holds the
-// forward's y = exp((z - zc) / tau) in fp16 (zc = zmax[i][chunk], the largest
-// raw logit of the 32-column chunk), so q = y exp(zc / tau - lse) and
-// G = s (q - scatter p) with s = g / N_valid / tau; G replaces y as bf16.
-// A task is one warp on GRAD_SEG columns of a row (so that a chunk still keeps
-// every SM's memory pipes full), GRAD_U x 256 columns at a time, 8 per lane,
-// each lane reading and writing its own 16 bytes.  The cached entries are
-// walked in ascending order and subtracted from the owning lane's value one
-// slot at a time (a repeated index subtracts each slot's p).
-// Rows from the valid count up to the next multiple of 64 (within the
-// buffer's c_cap rows) get G = 0: the dW contraction reads whole 64-row steps
-// of G against zero rows of h_c^T, and the y left there (invalid rows' logits)
-// would otherwise add nonzero terms.
-constexpr int GRAD_WARPS = 8;
-constexpr int GRAD_U = 4;
-constexpr int GRAD_SEG = 16 * GRAD_U * 256;  // columns per task
-
-__global__ void __launch_bounds__(32 * GRAD_WARPS)
-    kd_grad_rows_kernel(__nv_bfloat16* __restrict__ gbuf, int V, const float* __restrict__ zmax,
-                        int64_t zmax_ld, int c0, int c_cap, const int* __restrict__ rowmap,
-                        const int* __restrict__ nvalid, const int* __restrict__ sidx,
-                        const float* __restrict__ sp, int K, const float* __restrict__ lse,
-                        float grad_loss, float inv_tau, float c_log2) {
+// Single sweep, before the chunk's logit GEMM: one warp per local row i < cap
+// copies hc[i] = h[rowmap[c0 + i]] and, for the chunk's valid rows (i below
+// clamp(*nvalid - c0, 0, cap)), forms the row's offset roff[i] = h_t . W[v],
+// the student's logit at the teacher's highest cached entry v (the first
+// slot among equal teacher logits).  It is a logit of the row, so the
+// largest stored value exp((z - o) / tau) is at least about 1 and none of the
+// row's significant values underflows.  d8 = d / 8 (uint4 = 8 bf16).
+__global__ void kd_gather_rows_offset_kernel(const uint4* __restrict__ h,
+                                             const uint4* __restrict__ W,
+                                             const int* __restrict__ rowmap,
+                                             const int* __restrict__ nvalid,
+                                             const int* __restrict__ tidx,
+                                             const float* __restrict__ tlog, int K, int V, int c0,
+                                             int cap, int d8, uint4* __restrict__ hc,
+                                             float* __restrict__ roff) {
   const int lane = threadIdx.x & 31;
-  const int nseg = (V + GRAD_SEG - 1) / GRAD_SEG;
-  const int64_t wg = static_cast<int64_t>(blockIdx.x) * GRAD_WARPS + (threadIdx.x >> 5);
-  const int i = static_cast<int>(wg / nseg);  // row of the chunk
-  const int v0 = static_cast<int>(wg - static_cast<int64_t>(i) * nseg) * GRAD_SEG;
-  const int v1 = min(V, v0 + GRAD_SEG);
-  const int nv = *nvalid;
-  const int rows = max(0, min(nv - c0, c_cap));  // valid rows of the chunk
-  uint4* g = reinterpret_cast<uint4*>(gbuf + static_cast<int64_t>(i) * V);  // 8 elements each
-  if (i >= rows) {  // whole warp
-    if (i < min(c_cap, (rows + 63) & ~63))
-      for (int col = v0 + 8 * lane; col < v1; col += 256) g[col >> 3] = make_uint4(0u, 0u, 0u, 0u);
+  const int i = static_cast<int>((static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  if (i >= cap) return;  // whole warp
+  const int rows = max(0, min(*nvalid - c0, cap));
+  const int64_t t = rowmap[c0 + i];
+  const uint4* hr = h + t * d8;
+  uint4* out = hc + static_cast<int64_t>(i) * d8;
+  if (i >= rows) {
+    for (int j = lane; j < d8; j += 32) out[j] = hr[j];
     return;
   }
-  const int64_t t = rowmap[c0 + i];
-  const float sc = grad_loss / static_cast<float>(nv) * inv_tau;
-  const float lb = lse[t] * LOG2E;
-  const float* zrow = zmax + static_cast<int64_t>(i) * zmax_ld;
-  const int* srow = sidx + t * K;
-  const float* prow = sp + t * K;
-  int pos = lower_bound_row(srow, K, v0);
-  int nxt = pos < K ? __ldg(srow + pos) : INT_MAX;
-  for (int b0 = v0; b0 < v1; b0 += GRAD_U * 256) {
-    uint4 v[GRAD_U];
-    float f[GRAD_U];
-#pragma unroll
-    for (int u = 0; u < GRAD_U; ++u) {
-      const int col = b0 + u * 256 + 8 * lane;
-      if (col < V) {  // V % 8 == 0: a group is wholly inside or outside
-        v[u] = __ldcs(g + (col >> 3));
-        f[u] = sc * ex2f(fmaf(__ldg(zrow + (col >> 5)), c_log2, -lb));  // s exp(zc/tau - lse)
-      } else {
-        v[u] = make_uint4(0u, 0u, 0u, 0u);
-        f[u] = 0.f;
-      }
+  float best = -CUDART_INF_F;
+  int bk = K;
+  for (int k = lane; k < K; k += 32) {
+    const float x = tlog[t * K + k];
+    if (x > best) {  // ascending k: the first of equal logits stays
+      best = x;
+      bk = k;
     }
-    float gg[GRAD_U][8];
+  }
 #pragma unroll
-    for (int u = 0; u < GRAD_U; ++u) {
-      const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&w4[j]));
-        gg[u][2 * j] = f[u] * y.x;
-        gg[u][2 * j + 1] = f[u] * y.y;
-      }
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, best, o);
+    const int ok = __shfl_xor_sync(0xffffffffu, bk, o);
+    if (ob > best || (ob == best && ok < bk)) {
+      best = ob;
+      bk = ok;
     }
-    const int be = b0 + GRAD_U * 256;
-    while (nxt < be) {  // warp-uniform: every lane walks the same row
-      const int off = nxt - b0;
-      const int uu = off >> 8, ln = (off >> 3) & 31, jj = off & 7;
-      const float add = -(sc * __ldg(prow + pos));
-      if (lane == ln) {
+  }
+  const int v = min(max(tidx[t * K + (bk < K ? bk : 0)], 0), V - 1);  // in range even for bad input
+  const uint4* wr = W + static_cast<int64_t>(v) * d8;
+  float acc = 0.f;
+  for (int j = lane; j < d8; j += 32) {
+    const uint4 a = hr[j];
+    out[j] = a;
+    const uint4 b = __ldg(wr + j);
+    const uint32_t aa[4] = {a.x, a.y, a.z, a.w}, bb[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int u = 0; u < GRAD_U; ++u)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) gg[u][j] = (u == uu && j == jj) ? gg[u][j] + add : gg[u][j];
-      }
-      ++pos;
-      nxt = pos < K ? __ldg(srow + pos) : INT_MAX;
+    for (int q = 0; q < 4; ++q) {
+      const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aa[q]));
+      const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bb[q]));
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
     }
+  }
 #pragma unroll
-    for (int u = 0; u < GRAD_U; ++u) {
-      const int col = b0 + u * 256 + 8 * lane;
-      if (col < V) {
-        uint4 pk;
-        __nv_bfloat162 b0v = __floats2bfloat162_rn(gg[u][0], gg[u][1]);
-        __nv_bfloat162 b1v = __floats2bfloat162_rn(gg[u][2], gg[u][3]);
-        __nv_bfloat162 b2v = __floats2bfloat162_rn(gg[u][4], gg[u][5]);
-        __nv_bfloat162 b3v = __floats2bfloat162_rn(gg[u][6], gg[u][7]);
-        pk.x = *reinterpret_cast<uint32_t*>(&b0v);
-        pk.y = *reinterpret_cast<uint32_t*>(&b1v);
-        pk.z = *reinterpret_cast<uint32_t*>(&b2v);
-        pk.w = *reinterpret_cast<uint32_t*>(&b3v);
-        g[col >> 3] = pk;
-      }
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) roff[i] = acc;
+}
+
+// Single sweep, after the combine: completes the chunk's stored values so that
+// G = rscale times them.  At each distinct cached column v of a valid local row
+// i (original row t) the value becomes exp((z_v - o) / tau) - P exp(lse - o/tau),
+// P the teacher probability summed over the slots naming v, from the fp32
+// z_v / tau of the gather (one rounding to bf16, as for G itself).  Rows from
+// the valid count up to the next multiple of 64 (within c_cap) are set to 0:
+// the dW contraction reads whole 64-row steps of the buffer against zero rows
+// of h_c^T, and what an earlier chunk left there must not add NaN.  A chunk
+// flagged by the logit GEMM (ovf) has its G recomputed whole before this
+// kernel, which then only writes the zero rows.  One warp per row, the lanes
+// over the row's sorted slots (a repeated index is handled by the first slot
+// of its run, so no two lanes write one column).
+constexpr int FIX_WARPS = 8;
+
+__global__ void __launch_bounds__(32 * FIX_WARPS)
+    kd_fix_cached_kernel(__nv_bfloat16* __restrict__ gbuf, int V, int c0, int c_cap,
+                         const int* __restrict__ rowmap, const int* __restrict__ nvalid,
+                         const int* __restrict__ sidx, const float* __restrict__ sp,
+                         const float* __restrict__ zg, int K, const float* __restrict__ lse,
+                         const float* __restrict__ roff, float inv_tau,
+                         const int* __restrict__ ovf) {
+  const int rows = max(0, min(*nvalid - c0, c_cap));
+  const int tail_end = min(c_cap, (rows + 63) & ~63);
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t n16 = static_cast<int64_t>(tail_end - rows) * (V / 8);  // V % 8 == 0
+  uint4* tail = reinterpret_cast<uint4*>(gbuf + static_cast<int64_t>(rows) * V);
+  for (int64_t e = tid; e < n16; e += nthreads) tail[e] = make_uint4(0u, 0u, 0u, 0u);
+  if (*ovf) return;
+  const int lane = threadIdx.x & 31;
+  for (int64_t i = tid >> 5; i < rows; i += nthreads >> 5) {
+    const int64_t t = rowmap[c0 + i];
+    const float oi = roff[i] * inv_tau;
+    const float e2 = expf(lse[t] - oi);
+    const int* srow = sidx + t * K;
+    const float* prow = sp + t * K;
+    const float* zrow = zg + t * K;
+    __nv_bfloat16* grow = gbuf + i * V;
+    for (int k = lane; k < K; k += 32) {
+      const int v = srow[k];
+      if ((k > 0 && srow[k - 1] == v) || v < 0 || v >= V) continue;
+      float P = prow[k];
+      for (int q = k + 1; q < K && srow[q] == v; ++q) P += prow[q];
+      grow[v] = __float2bfloat16_rn(expf(zrow[k] - oi) - P * e2);
     }
   }
 }

@@ -146,17 +146,22 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
  * chunk by chunk with memory bounded by one chunk), in a single sweep that
  * computes each row's logits once instead of twice.  Rows are taken in the
  * order valid rows, then invalid rows; per chunk of `chunk` rows of that order
- * the logit GEMM forms the lse partials and the gather and also stores every
- * valid row's logits as fp16 values exp((z - zc) / tau) relative to the
- * largest raw logit zc of their 32-column chunk (and those zc) into the
- * chunk's G buffer (chunk x V x 2 bytes, as in kd_topk_kl_backward); the
- * chunk's lse and row_kl follow, a gradient pass turns the stored values into
- * bf16 G in place, and the chunk's dh and dW contractions consume it.  No
- * T x V buffer exists at any time.
+ * each valid row gets an offset o (the student's logit at the teacher's
+ * highest cached entry), and the logit GEMM forms the lse partials and the
+ * gather and also stores every valid row's logits as bf16 values
+ * exp((z - o) / tau) into the chunk's G buffer (chunk x V x 2 bytes, as in
+ * kd_topk_kl_backward).  With the chunk's lse, G = s exp(o / tau - lse) times
+ * those values away from the cached columns, which a small pass rewrites; the
+ * dh contraction applies the per-row factor to its output and the dW
+ * contraction takes it inside h_c^T (rounded to bf16).  A chunk in which some
+ * row's largest logit lies more than 64 ln 2 tau above its offset (the stored
+ * values would leave the range those steps can carry) has its G recomputed
+ * from the lse by the backward's logit GEMM instead; that launch returns at
+ * once for the other chunks.  No T x V buffer exists at any time.
  *
  * Results: loss, lse and row_kl equal kd_topk_kl_forward's bit for bit; dh and
- * dW equal kd_topk_kl_backward's to within bf16 rounding of G (the relative
- * logit's fp16 rounding, 2^-11, comes before it).
+ * dW equal kd_topk_kl_backward's to within bf16 rounding (G is rounded once on
+ * either route, at a different scale, and dW's h_c^T once more here).
  *
  * grad_loss: d(objective)/d(loss), as in kd_topk_kl_backward.
  * flags: 0 or KD_ACCUMULATE_DW.  With KD_ACCUMULATE_DW, dW += G^T h instead of
@@ -170,8 +175,8 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
  * Workspace bytes (*bytes) and number of kernel launches (*launches, the
  * status/counter resets and the dh zeroing are cudaMemsetAsync calls and are
  * not counted) of kd_topk_kl_forward_backward at this shape; either pointer
- * may be NULL.  About chunk * (2 V + V / 8) bytes plus O(T K) tables and the
- * backward's chunk buffers.
+ * may be NULL.  About 2 chunk V bytes plus O(T K) tables and the backward's
+ * chunk buffers.
  * Host-only; KD_ERR_INVALID_ARG / KD_ERR_UNSUPPORTED on bad shapes.
  */
 int kd_topk_kl_forward_backward_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K,
@@ -374,17 +379,19 @@ int kd_topk_kl_forward_noalloc(const void* h, const void* W, const int32_t* teac
  *   KD_KERNEL_TOPK_PASS1  teacher top-K producer: logits, tile maxima, lse partials
  *   KD_KERNEL_TOPK_SCAN   teacher top-K producer: candidate scan of the stored
  *                         logits (a SIMT kernel, timed the same way)
- *   KD_KERNEL_GRAD_PASS   single sweep (kd_topk_kl_forward_backward): G from the
- *                         stored logits (a SIMT kernel); that entry's logit GEMM
- *                         is timed as KD_KERNEL_LOGITS_FWD
+ *   KD_KERNEL_SWEEP_FIX   single sweep (kd_topk_kl_forward_backward): the pass
+ *                         that writes G's cached columns into the stored values
+ *                         (a SIMT kernel); that entry's logit GEMM is timed as
+ *                         KD_KERNEL_LOGITS_FWD and its recompute of a flagged
+ *                         chunk's G as KD_KERNEL_LOGITS_BWD
  *
  * kd_timing_start(capacity): creates 2 x capacity CUDA events on the current
  *   device (no device memory is allocated) and starts recording: from then on
  *   every launch of an id above that the entry points make (the contractions
  *   of the loss entries and of kd_teacher_topk, the producer's candidate scan
- *   and the single sweep's gradient pass), from any host thread, is bracketed by an event pair recorded on its
- *   stream, until `capacity` launches have been recorded.  Restarting discards
- *   earlier records.
+ *   and the single sweep's cached-column pass), from any host thread, is
+ *   bracketed by an event pair recorded on its stream, until `capacity`
+ *   launches have been recorded.  Restarting discards earlier records.
  * kd_timing_stop(): stops recording; the records stay readable.
  * kd_timing_query(kernel, *launches, *total_ms): waits for the recorded
  *   launches of that kernel id and returns their count and summed duration.
@@ -398,7 +405,7 @@ enum {
   KD_KERNEL_DW = 4,
   KD_KERNEL_TOPK_PASS1 = 5,
   KD_KERNEL_TOPK_SCAN = 6,
-  KD_KERNEL_GRAD_PASS = 7
+  KD_KERNEL_SWEEP_FIX = 7
 };
 int kd_timing_start(int32_t capacity);
 int kd_timing_stop(void);

@@ -159,18 +159,19 @@ def test_forward_backward_argument_checks():
 
 def test_forward_backward_workspace_and_launch_count():
     """The single sweep needs the backward's buffers (its bf16 G chunk holds
-    the forward's relative logits first) plus the forward's tables for one
-    chunk and the largest logit of every (row, 32-column chunk), and makes
-    2 + chunks x (7 or 8) + 2 launches."""
+    the forward's stored logits first) plus the gathered logits and the row
+    tables (T x K and T floats), one chunk's lse partials, three floats per
+    chunk row (offsets and scales) and one flag per chunk, and makes
+    2 + chunks x (8 or 9) + 2 launches."""
     T, V, d, K = 32768, 201088, 2880, 100
     for chunk in (4096, 8192):
         f, b = kd.kd_topk_kl_workspace_size(T, V, d, K, chunk)
         sw, n = kd.kd_topk_kl_forward_backward_workspace_size(T, V, d, K, chunk)
         extra = sw - b
-        nch = -(-V // 32)
-        assert chunk * nch * 4 <= extra <= chunk * nch * 4 + T * K * 4 + 786 * chunk * 4 + T * 4 + 4096
+        tables = T * K * 4 + 786 * chunk * 4 + T * 4 + 3 * chunk * 4
+        assert tables <= extra <= tables + 4096
         chunks = -(-T // chunk)
-        assert n in (2 + chunks * 7 + 2, 2 + chunks * 8 + 2)
+        assert n in (2 + chunks * 8 + 2, 2 + chunks * 9 + 2)
     with pytest.raises(kd.KDError):
         kd.kd_topk_kl_forward_backward_workspace_size(0, V, d, K, 64)
     with pytest.raises(kd.KDError):

@@ -125,7 +125,7 @@ def test_ctx_32k_full_forward_sampled_grads():
     for k in ("loss", "lse", "row_kl"):
         np.testing.assert_array_equal(sw[k], gpu[k], err_msg=k)
     _sampled_grads(w, sw, P, f, seed=2, n_rows=512, n_vrows=640, slab=256)
-    assert rel_l2(sw["dh"], gpu["dh"]) <= 2e-3 and rel_l2(sw["dW"], gpu["dW"]) <= 2e-3
+    assert rel_l2(sw["dh"], gpu["dh"]) <= 5e-3 and rel_l2(sw["dW"], gpu["dW"]) <= 5e-3
     del sw
     # every row of G sums to zero, so the column sums of dW vanish up to the
     # bf16 rounding of G (a property beside the oracle comparison above)
