@@ -30,7 +30,8 @@ __all__ = [
     "kd_topk_kl_workspace_size", "kd_topk_kl_launch_count", "kd_topk_kl_forward",
     "kd_topk_kl_forward_backward_workspace_size",
     "kd_topk_kl_forward_noalloc", "kd_topk_kl_backward", "kd_topk_kl_forward_backward",
-    "KD_ACCUMULATE_DW", "kd_entropy_filter_workspace_size", "kd_entropy_filter",
+    "KD_ACCUMULATE_DW", "KD_VALID_ROWS_ONLY", "kd_entropy_filter_workspace_size",
+    "kd_entropy_filter",
     "kd_topk_kl_forward_residual", "kd_topk_kl_backward_residual",
     "kd_teacher_topk_workspace_size", "kd_teacher_topk", "PRODUCER_KERNELS",
     "kd_gemm_bf16_diag", "kd_gemm_bf16_diag_pair", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
@@ -46,6 +47,7 @@ PRODUCER_KERNELS = {"topk_pass1": 5, "topk_scan": 6}
 
 KD_OK = 0
 KD_ACCUMULATE_DW = 1
+KD_VALID_ROWS_ONLY = 2
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB = None
 
@@ -230,7 +232,8 @@ def kd_topk_kl_backward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, ls
 def kd_topk_kl_forward_backward(h, W, teacher_idx, teacher_logits, valid, tau, chunk, grad_loss,
                                 loss, lse, dh, dW, row_kl=None, *, flags=0, ws, dev_status,
                                 stream=None):
-    """Forward + backward in one call (one teacher prep); flags: KD_ACCUMULATE_DW."""
+    """Forward + backward in one call (one teacher prep); flags: KD_ACCUMULATE_DW,
+    KD_VALID_ROWS_ONLY."""
     T, d = h.shape
     V = W.shape[0]
     K = teacher_idx.shape[1]
@@ -463,7 +466,7 @@ class TopKKL:
         return self.loss
 
     def forward_backward(self, h, W, idx, tl, valid, tau, grad_loss=1.0, accumulate_dW=False,
-                         row_kl=True, stream=None):
+                         row_kl=True, stream=None, valid_rows_only=False):
         ws = self.ws
         if ws.numel() < self.sweep_bytes:
             if self._ws_sweep is None:
@@ -473,7 +476,8 @@ class TopKKL:
         kd_topk_kl_forward_backward(h, W, idx, tl, valid, tau, self.chunk, grad_loss, self.loss,
                                     self.lse, self.dh, self.dW,
                                     self.row_kl if row_kl else None,
-                                    flags=KD_ACCUMULATE_DW if accumulate_dW else 0, ws=ws,
+                                    flags=(KD_ACCUMULATE_DW if accumulate_dW else 0)
+                                    | (KD_VALID_ROWS_ONLY if valid_rows_only else 0), ws=ws,
                                     dev_status=self.status, stream=stream)
         return self.loss, self.dh, self.dW
 

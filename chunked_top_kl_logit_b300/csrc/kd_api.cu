@@ -756,7 +756,7 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
 int enqueue_sweep(const void* h, const void* W, const int32_t* teacher_idx,
                   const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
                   int64_t d, int32_t K, float tau, const Layout& L, void* ws, const Ws& w,
-                  int sms, float grad_loss, int accumulate_dW, float* loss,
+                  int sms, float grad_loss, int accumulate_dW, int valid_only, float* loss,
                   float* lse, float* row_kl, float* dh, float* dW, int32_t* dev_status,
                   cudaStream_t st) {
   int rc = KD_OK;
@@ -819,10 +819,17 @@ int enqueue_sweep(const void* h, const void* W, const int32_t* teacher_idx,
     p.rowmap_base = static_cast<int>(c0);
     p.roff = roff;
     p.ovf = flag;
+    if (valid_only) {  // only the chunk's valid rows (the first ones of the row order)
+      p.dyn_count = w.nvalid;
+      p.dyn_base = static_cast<int>(c0);
+      p.dyn_cap = static_cast<int>(M);
+      p.dyn_kind = 1;
+    }
     if ((rc = launch_gemm<EPI_FWDZ>(ta, tb, ty, ta, p, sms, st))) return rc;
 
     // (2) lse and row_kl of the chunk's rows, and the scales of the stored values
-    const SweepScales sc{roff, flag, w.nvalid, grad_loss, inv_tau, rscale, escale, oscale};
+    const SweepScales sc{roff, flag, w.nvalid, grad_loss, inv_tau, rscale, escale, oscale,
+                         valid_only};
     kd_combine_kernel<<<static_cast<unsigned>(cdiv(M, 32)), dim3(32, COMBINE_SPLIT), 0, st>>>(
         part, C, p.n_tiles, static_cast<int>(M), K, rowmap, static_cast<int>(c0), w.sidx, w.sp,
         zg, w.tterm, nullptr, valid, lse, rkl, nullptr, nullptr, sc);
@@ -944,7 +951,8 @@ int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* tea
                         dev_status);
   if (rc != KD_OK) return rc;
   if (!loss || !lse || !dh || !dW || !aligned16(dh) || !aligned16(dW)) return KD_ERR_INVALID_ARG;
-  if (!std::isfinite(grad_loss) || (flags & ~static_cast<uint32_t>(KD_ACCUMULATE_DW)))
+  if (!std::isfinite(grad_loss) ||
+      (flags & ~static_cast<uint32_t>(KD_ACCUMULATE_DW | KD_VALID_ROWS_ONLY)))
     return KD_ERR_INVALID_ARG;
   const Layout L = make_layout(T, V, d, K, chunk, true);
   if (ws_bytes < L.bwd_total) return KD_ERR_WORKSPACE;
@@ -958,8 +966,9 @@ int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* tea
                      st)))
     return rc;
   return enqueue_sweep(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, L, ws, w, sms,
-                       grad_loss, (flags & KD_ACCUMULATE_DW) ? 1 : 0, loss, lse, row_kl, dh, dW,
-                       dev_status, st);
+                       grad_loss, (flags & KD_ACCUMULATE_DW) ? 1 : 0,
+                       (flags & KD_VALID_ROWS_ONLY) ? 1 : 0, loss, lse, row_kl, dh, dW, dev_status,
+                       st);
 }
 
 int kd_gemm_bf16_diag(const void* A, const void* B, float* C, int64_t M, int64_t N, int64_t Kd,

@@ -1133,7 +1133,9 @@ __device__ __forceinline__ float merge_lse(const float (&sm)[COMBINE_SPLIT][32],
 // count: escale[i] = exp(o_i / tau - lse) and rscale[i] = s escale[i], with
 // s = grad_loss / N_valid / tau, so that G = rscale times the stored values;
 // *oscale = s.  When the chunk is flagged (ovf), its G is recomputed whole and
-// the scales are 1.  Rows past the valid count get 0.
+// the scales are 1.  Rows past the valid count get 0.  valid_only: the logit
+// GEMM covered the chunk's valid rows only, so the other rows get lse = NaN and
+// row_kl = 0 without reading partials.
 struct SweepScales {
   const float* roff;
   const int* ovf;
@@ -1142,6 +1144,7 @@ struct SweepScales {
   float* rscale;
   float* escale;
   float* oscale;
+  int valid_only;
 };
 
 __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
@@ -1162,10 +1165,12 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
   const bool in = li < T;
   const int row = (in && rowmap) ? rowmap[rowmap_base + li] : li;
   const int64_t rk0 = static_cast<int64_t>(row) * K;
+  // a row whose logits were formed (all rows unless valid_only)
+  const bool live = in && !(sw.valid_only && li >= *sw.nvalid - rowmap_base);
   // online logsumexp over this thread's tiles
   float m = -CUDART_INF_F;
   float s = 0.f;
-  if (in)
+  if (live)
     for (int j = y; j < n_tiles; j += COMBINE_SPLIT)
       online_lse_add(part[static_cast<int64_t>(j) * part_ld + li], m, s);
   sm[y][x] = m;
@@ -1174,7 +1179,7 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
   if (y == 0) {
     const float L = merge_lse(sm, ss, x);
     s_lse[x] = L;
-    if (in && lse_out && !resid) lse_out[row] = L;
+    if (in && lse_out && !resid) lse_out[row] = live ? L : CUDART_NAN_F;
     if (sw.rscale) {  // uniform
       const int nv = *sw.nvalid;
       const bool redo = *sw.ovf != 0;
@@ -1214,7 +1219,7 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
   const float lse = s_lse[x];
   // this thread's share of sum_k p_k (lse - zg_k) and of the repeated slots' mass
   float acc = 0.f, mass = 0.f;
-  if (in) {
+  if (live) {
     for (int k = y; k < K; k += COMBINE_SPLIT) {
       const float zk = zg[rk0 + k];
       acc += sp[rk0 + k] * (lse - zk);
@@ -1240,7 +1245,7 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
         if (outside_mass_out) outside_mass_out[row] = Q;
       }
       float rk = 0.f;
-      if (valid[row]) {
+      if (live && valid[row]) {
         rk = tterm[row] + a;
         if (resid) {
           const float R = resid[row];

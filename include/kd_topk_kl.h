@@ -164,13 +164,17 @@ int kd_topk_kl_backward(const void* h, const void* W, const int32_t* teacher_idx
  * either route, at a different scale, and dW's h_c^T once more here).
  *
  * grad_loss: d(objective)/d(loss), as in kd_topk_kl_backward.
- * flags: 0 or KD_ACCUMULATE_DW.  With KD_ACCUMULATE_DW, dW += G^T h instead of
- *   dW = G^T h (gradient accumulation over micro-batches); dh is always
- *   overwritten.
+ * flags: 0, KD_ACCUMULATE_DW, KD_VALID_ROWS_ONLY or both.  With
+ *   KD_ACCUMULATE_DW, dW += G^T h instead of dW = G^T h (gradient accumulation
+ *   over micro-batches); dh is always overwritten.  With KD_VALID_ROWS_ONLY the
+ *   logits of rows with valid = 0 are not formed at all (they add nothing to
+ *   the loss or the gradients): their lse is written as NaN and their row_kl
+ *   as 0; everything else is as without the flag, bit for bit.
  * Outputs (device): loss, lse (required), row_kl (or NULL), dh, dW.
  * ws/ws_bytes: at least *bytes of kd_topk_kl_forward_backward_workspace_size.
  */
 #define KD_ACCUMULATE_DW 1u
+#define KD_VALID_ROWS_ONLY 2u
 /*
  * Workspace bytes (*bytes) and number of kernel launches (*launches, the
  * status/counter resets and the dh zeroing are cudaMemsetAsync calls and are

@@ -152,7 +152,7 @@ def test_forward_backward_argument_checks():
     args = lambda flags, lse, ws_bytes: (A, A, A, A, A, T, V, d, K, 1.0, chunk, 1.0, flags,
                                          A, lse, None, A, A, A, ws_bytes, A, None)
     sw, _ = kd.kd_topk_kl_forward_backward_workspace_size(T, V, d, K, chunk)
-    assert L.kd_topk_kl_forward_backward(*args(2, A, sw)) == INVALID
+    assert L.kd_topk_kl_forward_backward(*args(4, A, sw)) == INVALID
     assert L.kd_topk_kl_forward_backward(*args(0, None, sw)) == INVALID
     assert L.kd_topk_kl_forward_backward(*args(0, A, sw - 1)) == WORKSPACE
 

@@ -197,3 +197,35 @@ def test_sweep_stored_value_range(name, wscale, hscale):
         assert np.all(np.isfinite(got)), k
         assert rel_l2(got, ref) <= GRAD_RL2, k
         assert rel_l2(got, getattr(a, k).double().cpu().numpy()) <= SWEEP_RL2, k
+
+
+@pytest.mark.parametrize("chunk", [128, 250])
+def test_valid_rows_only(chunk):
+    """KD_VALID_ROWS_ONLY forms no logits for masked rows: their lse is NaN and
+    their row_kl 0; the loss, the valid rows' lse and row_kl, dh and dW are bit
+    for bit those of the step without the flag (chunk 250 leaves the masked rows
+    of the row order spread over the last two chunks, and one chunk of
+    masked rows only)."""
+    x = make_inputs(workload("small_4k", T=600, d=192, V=3000, K=30, tau=1.0,
+                             mask_kind="packed", seq_len=150, pad=40))
+    g = to_device(x)
+    T, d = g["h"].shape
+    V, K = g["W"].shape[0], g["teacher_idx"].shape[1]
+    args = (g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"], g["tau"], 0.5)
+    a = kd.TopKKL(T, V, d, K, chunk, fused=True)
+    a.forward_backward(*args)
+    b = kd.TopKKL(T, V, d, K, chunk, fused=True)
+    b.forward_backward(*args, valid_rows_only=True)
+    torch.cuda.synchronize()
+    kd.check_device_status(a.status, "all rows")
+    kd.check_device_status(b.status, "valid rows only")
+    v = g["valid"] != 0
+    assert int((~v).sum()) == 4 * 40
+    assert torch.equal(a.loss, b.loss)
+    assert torch.equal(a.lse[v], b.lse[v]) and bool(torch.isnan(b.lse[~v]).all())
+    assert torch.equal(a.row_kl, b.row_kl) and bool((b.row_kl[~v] == 0).all())
+    assert torch.equal(a.dh, b.dh) and torch.equal(a.dW, b.dW)
+    P = oracle_inputs(x)
+    f = O.forward(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], P["valid"], P["tau"])
+    assert abs(float(b.loss.item()) - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert np.abs(b.lse[v].double().cpu().numpy() - f["lse"][P["valid"] != 0]).max() <= LSE_ATOL
