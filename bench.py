@@ -2,9 +2,10 @@
 """Benchmark of the fused top-K KL distillation loss, forward + backward.
 
 One step = one kd_topk_kl_forward_backward call over one synthetic batch (the
-single-sweep training step: teacher prep, then per row chunk the logit GEMM with
-online lse + gather that also stores the chunk's fp32 logits, the combine, the
-gradient pass, the dh and dW contractions); `--api split` times
+single-sweep training step: teacher prep, then per row chunk the row offsets, the
+logit GEMM with online lse + gather that also stores the valid rows' logits as
+bf16 values relative to their offsets, the combine, the cached-column pass, the
+dh and dW contractions); `--api split` times
 kd_topk_kl_forward + kd_topk_kl_backward instead (the backward recomputes the
 logits).  Default workload: ctx_32k (T=32768, V=201088, d=2880,
 K=100, tau=1, 10% rows masked), inputs resident in HBM and larger than L2.

@@ -50,7 +50,8 @@ constexpr float LN2 = 0.6931471805599453f;
 // EPI_FWD_RESID: the forward of the residual-mass variant, whose lse partials
 // cover only the columns outside the row's cache.  EPI_FWDZ: the forward of
 // the single-sweep training step on one chunk of rows (valid rows first),
-// which also stores the chunk's fp32 logits for the gradient pass.
+// which also stores the valid rows' logits as bf16 exp((z - o) / tau) for the
+// gradient contractions.
 enum EpiMode {
   EPI_FWD = 0,
   EPI_DZ = 1,
@@ -451,7 +452,7 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
     // The chunk's largest raw logit zc inside the vocabulary (c > 0, so c zc is
     // the largest scaled one), then y_j = 2^(c z_j - c zc) in (0, 1]: one FFMA
     // and one ex2 per element give the lse term and, in the single sweep, the
-    // stored relative logit.  The rounding is pinned (explicit _rn operations),
+    // stored value.  The rounding is pinned (explicit _rn operations),
     // so that the sweep's lse equals the plain forward's bit for bit.
     const bool full = cb + 32 <= p.N;  // uniform: all 32 columns inside the vocabulary
     float zc = -CUDART_INF_F;
