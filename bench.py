@@ -377,7 +377,7 @@ def run_ours(args, w, world, rank, local_rank):
     torch.cuda.reset_peak_memory_stats(dev)
     free_before = torch.cuda.mem_get_info(dev)[0]  # cross-check with the CUDA device's free-memory count
     residual = args.variant == "residual"
-    fused = args.api == "fused" and not residual  # the residual variant has split entries only
+    fused = args.api == "fused"
     m = kd.TopKKL(T, V, d, K, chunk, device=dev, fused=fused)
     if residual:
         from synth import teacher_full_lse
@@ -385,7 +385,10 @@ def run_ours(args, w, world, rank, local_rank):
         outside_mass = torch.empty(T, dtype=torch.float32, device=dev)
 
     def fwd_part():
-        if residual:
+        if residual and fused:
+            m.forward_backward_residual(h, W, idx, tl, tlse, valid, tau, 1.0,
+                                        valid_rows_only=args.valid_rows_only)
+        elif residual:
             kd.kd_topk_kl_forward_residual(h, W, idx, tl, tlse, valid, tau, chunk, m.loss, m.lse,
                                            m.row_kl, outside_mass, ws=m.ws, dev_status=m.status)
         elif fused:
@@ -395,7 +398,7 @@ def run_ours(args, w, world, rank, local_rank):
             m.forward(h, W, idx, tl, valid, tau)
 
     def bwd_part():
-        if residual:
+        if residual and not fused:
             kd.kd_topk_kl_backward_residual(h, W, idx, tl, tlse, valid, tau, chunk, m.lse,
                                             outside_mass, 1.0, m.dh, m.dW, ws=m.ws,
                                             dev_status=m.status)
@@ -476,7 +479,10 @@ def run_ours(args, w, world, rank, local_rank):
     dom = max(contractions, key=lambda k: kernels[k]["ms_per_step"])
     kd_dom = kernels[dom]
     dom_desc = KERNEL_DESC["logits_fwd_sweep" if (sweep and dom == "logits_fwd") else dom]
-    dom_id = 7 if (sweep and dom == "logits_fwd") else kd.KERNELS[dom]
+    if dom == "logits_fwd":  # the forward's epilogue mode: single sweep / residual variant
+        dom_id = (8 if residual else 7) if sweep else (6 if residual else 0)
+    else:
+        dom_id = kd.KERNELS[dom]
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": n,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,

@@ -33,6 +33,7 @@ __all__ = [
     "KD_ACCUMULATE_DW", "KD_VALID_ROWS_ONLY", "kd_entropy_filter_workspace_size",
     "kd_entropy_filter",
     "kd_topk_kl_forward_residual", "kd_topk_kl_backward_residual",
+    "kd_topk_kl_forward_backward_residual",
     "kd_teacher_topk_workspace_size", "kd_teacher_topk", "PRODUCER_KERNELS",
     "kd_gemm_bf16_diag", "kd_gemm_bf16_diag_pair", "kd_pipeline_wait_selftest", "check_device_status", "TopKKL",
     "KERNELS", "SWEEP_KERNELS", "kd_timing_start", "kd_timing_stop", "kd_timing_query", "kd_timing_release",
@@ -96,6 +97,10 @@ def lib() -> ctypes.CDLL:
         L.kd_topk_kl_backward_residual.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, f32,
                                                    i64, vp, vp, f32, vp, vp, vp, sz, vp, vp]
         L.kd_topk_kl_backward_residual.restype = ctypes.c_int
+        L.kd_topk_kl_forward_backward_residual.argtypes = [
+            vp, vp, vp, vp, vp, vp, i64, i64, i64, i32, f32, i64, f32, ctypes.c_uint32, vp, vp, vp,
+            vp, vp, vp, vp, sz, vp, vp]
+        L.kd_topk_kl_forward_backward_residual.restype = ctypes.c_int
         L.kd_teacher_topk_workspace_size.argtypes = [i64, i64, i64, i32, i64, ctypes.POINTER(sz)]
         L.kd_teacher_topk_workspace_size.restype = ctypes.c_int
         L.kd_teacher_topk.argtypes = [vp, vp, i64, i64, i64, i32, f32, i64, vp, vp, vp, vp, sz, vp,
@@ -244,6 +249,24 @@ def kd_topk_kl_forward_backward(h, W, teacher_idx, teacher_logits, valid, tau, c
         float(tau), int(chunk), float(grad_loss), int(flags), _ptr(loss), _ptr(lse), _ptr(row_kl),
         _ptr(dh), _ptr(dW), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status), st)
     _check(rc, "kd_topk_kl_forward_backward")
+
+
+def kd_topk_kl_forward_backward_residual(h, W, teacher_idx, teacher_logits, teacher_lse, valid,
+                                         tau, chunk, grad_loss, loss, lse, outside_mass, dh, dW,
+                                         row_kl=None, *, flags=0, ws, dev_status, stream=None):
+    """The residual-mass variant's forward + backward in one call (the single
+    sweep); flags: KD_ACCUMULATE_DW, KD_VALID_ROWS_ONLY."""
+    T, d = h.shape
+    V = W.shape[0]
+    K = teacher_idx.shape[1]
+    st = _stream(stream, h, W, teacher_idx, teacher_logits, teacher_lse, valid, loss, lse,
+                 outside_mass, row_kl, dh, dW, ws, dev_status)
+    rc = lib().kd_topk_kl_forward_backward_residual(
+        _ptr(h), _ptr(W), _ptr(teacher_idx), _ptr(teacher_logits), _ptr(teacher_lse), _ptr(valid),
+        T, V, d, K, float(tau), int(chunk), float(grad_loss), int(flags), _ptr(loss), _ptr(lse),
+        _ptr(row_kl), _ptr(outside_mass), _ptr(dh), _ptr(dW), _ptr(ws),
+        ws.numel() * ws.element_size(), _ptr(dev_status), st)
+    _check(rc, "kd_topk_kl_forward_backward_residual")
 
 
 def kd_topk_kl_forward_residual(h, W, teacher_idx, teacher_logits, teacher_lse, valid, tau, chunk,
@@ -465,20 +488,37 @@ class TopKKL:
                            dev_status=self.status, stream=stream)
         return self.loss
 
+    def _sweep_ws(self):
+        if self.ws.numel() >= self.sweep_bytes:
+            return self.ws
+        if self._ws_sweep is None:
+            self._ws_sweep = torch.empty(self.sweep_bytes, dtype=torch.uint8,
+                                         device=self.ws.device)
+        return self._ws_sweep
+
     def forward_backward(self, h, W, idx, tl, valid, tau, grad_loss=1.0, accumulate_dW=False,
                          row_kl=True, stream=None, valid_rows_only=False):
-        ws = self.ws
-        if ws.numel() < self.sweep_bytes:
-            if self._ws_sweep is None:
-                self._ws_sweep = torch.empty(self.sweep_bytes, dtype=torch.uint8,
-                                             device=self.ws.device)
-            ws = self._ws_sweep
         kd_topk_kl_forward_backward(h, W, idx, tl, valid, tau, self.chunk, grad_loss, self.loss,
                                     self.lse, self.dh, self.dW,
                                     self.row_kl if row_kl else None,
                                     flags=(KD_ACCUMULATE_DW if accumulate_dW else 0)
-                                    | (KD_VALID_ROWS_ONLY if valid_rows_only else 0), ws=ws,
-                                    dev_status=self.status, stream=stream)
+                                    | (KD_VALID_ROWS_ONLY if valid_rows_only else 0),
+                                    ws=self._sweep_ws(), dev_status=self.status, stream=stream)
+        return self.loss, self.dh, self.dW
+
+    def forward_backward_residual(self, h, W, idx, tl, teacher_lse, valid, tau, grad_loss=1.0,
+                                  accumulate_dW=False, row_kl=True, stream=None,
+                                  valid_rows_only=False):
+        """The residual-mass variant's training step; the student's mass outside
+        the cache lands in self.outside_mass."""
+        if getattr(self, "outside_mass", None) is None:
+            self.outside_mass = torch.empty_like(self.lse)
+        kd_topk_kl_forward_backward_residual(
+            h, W, idx, tl, teacher_lse, valid, tau, self.chunk, grad_loss, self.loss, self.lse,
+            self.outside_mass, self.dh, self.dW, self.row_kl if row_kl else None,
+            flags=(KD_ACCUMULATE_DW if accumulate_dW else 0)
+            | (KD_VALID_ROWS_ONLY if valid_rows_only else 0),
+            ws=self._sweep_ws(), dev_status=self.status, stream=stream)
         return self.loss, self.dh, self.dW
 
     def backward(self, h, W, idx, tl, valid, tau, grad_loss=1.0, stream=None):

@@ -271,7 +271,8 @@ template <int MODE>
 int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
                 const CUtensorMap& dm, GemmParams p, int sms, cudaStream_t st) {
   if (p.num_tiles <= 0) return KD_OK;
-  p.epi_smem = (MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX || MODE == EPI_FWDZ)
+  p.epi_smem = (MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX || MODE == EPI_FWDZ ||
+                MODE == EPI_FWDZ_RESID)
                    ? 4u * 2u * DW_PIECE_FLOATS * 4u
                    : 0u;
   // the stage ring shares the opt-in shared-memory limit with the staging
@@ -285,7 +286,10 @@ int launch_gemm(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c
   // the residual variant's and the single sweep's forwards are timed as the
   // forward logit kernel
   const int slot = MODE == EPI_STORE ? -1
-                   : timing_slot((MODE == EPI_FWD_RESID || MODE == EPI_FWDZ) ? EPI_FWD : MODE);
+                   : timing_slot((MODE == EPI_FWD_RESID || MODE == EPI_FWDZ ||
+                                  MODE == EPI_FWDZ_RESID)
+                                     ? EPI_FWD
+                                     : MODE);
   if (slot >= 0 && cudaEventRecord(timing().recs[static_cast<size_t>(slot)].start, st) != cudaSuccess)
     return KD_ERR_CUDA;
   kd_gemm_kernel<MODE><<<grid, NUM_THREADS, smem, st>>>(a, b, c, dm, p);
@@ -756,9 +760,9 @@ int enqueue_backward(const void* h, const void* W, const uint8_t* valid, int64_t
 int enqueue_sweep(const void* h, const void* W, const int32_t* teacher_idx,
                   const float* teacher_logits, const uint8_t* valid, int64_t T, int64_t V,
                   int64_t d, int32_t K, float tau, const Layout& L, void* ws, const Ws& w,
-                  int sms, float grad_loss, int accumulate_dW, int valid_only, float* loss,
-                  float* lse, float* row_kl, float* dh, float* dW, int32_t* dev_status,
-                  cudaStream_t st) {
+                  const Variant& var, int sms, float grad_loss, int accumulate_dW,
+                  int valid_only, float* loss, float* lse, float* row_kl, float* dh, float* dW,
+                  int32_t* dev_status, cudaStream_t st) {
   int rc = KD_OK;
   char* wb = static_cast<char*>(ws);
   int* rowmap = reinterpret_cast<int*>(wb + L.rowmap);
@@ -825,14 +829,18 @@ int enqueue_sweep(const void* h, const void* W, const int32_t* teacher_idx,
       p.dyn_cap = static_cast<int>(M);
       p.dyn_kind = 1;
     }
-    if ((rc = launch_gemm<EPI_FWDZ>(ta, tb, ty, ta, p, sms, st))) return rc;
+    rc = var.residual() ? launch_gemm<EPI_FWDZ_RESID>(ta, tb, ty, ta, p, sms, st)
+                        : launch_gemm<EPI_FWDZ>(ta, tb, ty, ta, p, sms, st);
+    if (rc) return rc;
 
-    // (2) lse and row_kl of the chunk's rows, and the scales of the stored values
+    // (2) lse and row_kl of the chunk's rows (and the mass outside the cache),
+    // and the scales of the stored values
+    const float* resid = var.residual() ? w.resid : nullptr;
     const SweepScales sc{roff, flag, w.nvalid, grad_loss, inv_tau, rscale, escale, oscale,
                          valid_only};
     kd_combine_kernel<<<static_cast<unsigned>(cdiv(M, 32)), dim3(32, COMBINE_SPLIT), 0, st>>>(
         part, C, p.n_tiles, static_cast<int>(M), K, rowmap, static_cast<int>(c0), w.sidx, w.sp,
-        zg, w.tterm, nullptr, valid, lse, rkl, nullptr, nullptr, sc);
+        zg, w.tterm, resid, valid, lse, rkl, var.outside_mass_out, nullptr, sc);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
 
     // (3) only for a flagged chunk: G of its valid rows recomputed from the lse
@@ -846,6 +854,8 @@ int enqueue_sweep(const void* h, const void* W, const int32_t* teacher_idx,
     q.inv_tau = inv_tau;
     q.c_log2 = LOG2E * inv_tau;
     q.lse = lse;
+    q.resid = resid;
+    q.outside_mass = var.outside_mass_out;
     q.valid = valid;
     q.nvalid = w.nvalid;
     q.grad_loss = grad_loss;
@@ -868,7 +878,8 @@ int enqueue_sweep(const void* h, const void* W, const int32_t* teacher_idx,
       return KD_ERR_CUDA;
     kd_fix_cached_kernel<<<static_cast<unsigned>(cdiv(C, FIX_WARPS)), 32 * FIX_WARPS, 0, st>>>(
         G, static_cast<int>(V), static_cast<int>(c0), static_cast<int>(C), rowmap, w.nvalid, w.sidx,
-        w.sp, zg, K, lse, roff, inv_tau, flag);
+        w.sp, zg, K, lse, roff, inv_tau, resid, var.outside_mass_out, flag, rscale, escale,
+        oscale);
     if (cudaGetLastError() != cudaSuccess) return KD_ERR_CUDA;
     if (slot >= 0 &&
         cudaEventRecord(timing().recs[static_cast<size_t>(slot)].stop, st) != cudaSuccess)
@@ -965,8 +976,8 @@ int kd_topk_kl_forward_backward(const void* h, const void* W, const int32_t* tea
   if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
                      st)))
     return rc;
-  return enqueue_sweep(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, L, ws, w, sms,
-                       grad_loss, (flags & KD_ACCUMULATE_DW) ? 1 : 0,
+  return enqueue_sweep(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, L, ws, w, var,
+                       sms, grad_loss, (flags & KD_ACCUMULATE_DW) ? 1 : 0,
                        (flags & KD_VALID_ROWS_ONLY) ? 1 : 0, loss, lse, row_kl, dh, dW, dev_status,
                        st);
 }
@@ -1186,6 +1197,42 @@ int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* te
     return rc;
   return enqueue_backward(h, W, valid, T, V, d, K, tau, L, ws, w, var, sms, lse, grad_loss, dh, dW,
                           0, dev_status, st);
+}
+
+int kd_topk_kl_forward_backward_residual(const void* h, const void* W, const int32_t* teacher_idx,
+                                         const float* teacher_logits, const float* teacher_lse,
+                                         const uint8_t* valid, int64_t T, int64_t V, int64_t d,
+                                         int32_t K, float tau, int64_t chunk, float grad_loss,
+                                         uint32_t flags, float* loss, float* lse, float* row_kl,
+                                         float* outside_mass, float* dh, float* dW, void* ws,
+                                         size_t ws_bytes, int32_t* dev_status,
+                                         struct CUstream_st* stream) {
+  int rc = check_inputs(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, chunk, ws,
+                        dev_status);
+  if (rc != KD_OK) return rc;
+  if (!loss || !lse || !outside_mass || !dh || !dW || !aligned16(dh) || !aligned16(dW) ||
+      !teacher_lse || (reinterpret_cast<uintptr_t>(teacher_lse) & 3u))
+    return KD_ERR_INVALID_ARG;
+  if (!std::isfinite(grad_loss) ||
+      (flags & ~static_cast<uint32_t>(KD_ACCUMULATE_DW | KD_VALID_ROWS_ONLY)))
+    return KD_ERR_INVALID_ARG;
+  const Layout L = make_layout(T, V, d, K, chunk, true);
+  if (ws_bytes < L.bwd_total) return KD_ERR_WORKSPACE;
+  int sms = 0;
+  if ((rc = device_sms(&sms)) != KD_OK) return rc;
+  if (!encode_fn()) return KD_ERR_CUDA;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const Ws w = carve(ws, L);
+  Variant var;
+  var.teacher_lse = teacher_lse;
+  var.outside_mass_out = outside_mass;
+  if ((rc = run_prep(teacher_idx, teacher_logits, valid, T, K, V, 1.0f / tau, w, var, dev_status,
+                     st)))
+    return rc;
+  return enqueue_sweep(h, W, teacher_idx, teacher_logits, valid, T, V, d, K, tau, L, ws, w, var,
+                       sms, grad_loss, (flags & KD_ACCUMULATE_DW) ? 1 : 0,
+                       (flags & KD_VALID_ROWS_ONLY) ? 1 : 0, loss, lse, row_kl, dh, dW,
+                       dev_status, st);
 }
 
 int kd_teacher_topk_workspace_size(int64_t T, int64_t V, int64_t d, int32_t K, int64_t chunk,

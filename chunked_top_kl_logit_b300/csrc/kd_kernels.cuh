@@ -51,7 +51,8 @@ constexpr float LN2 = 0.6931471805599453f;
 // cover only the columns outside the row's cache.  EPI_FWDZ: the forward of
 // the single-sweep training step on one chunk of rows (valid rows first),
 // which also stores the valid rows' logits as bf16 exp((z - o) / tau) for the
-// gradient contractions.
+// gradient contractions.  EPI_FWDZ_RESID: the same for the residual-mass
+// variant (lse partials over the columns outside the cache).
 enum EpiMode {
   EPI_FWD = 0,
   EPI_DZ = 1,
@@ -60,7 +61,8 @@ enum EpiMode {
   EPI_DW = 4,
   EPI_TMAX = 5,
   EPI_FWD_RESID = 6,
-  EPI_FWDZ = 7
+  EPI_FWDZ = 7,
+  EPI_FWDZ_RESID = 8
 };
 
 struct GemmParams {
@@ -144,6 +146,9 @@ struct GemmParams {
 // chunk is flagged for recompute: 2^64 keeps the values, the sums of the dh
 // contraction and the scales exp(o / tau - lse) inside fp32 / bf16 range.
 constexpr float YREL_MAX_LOG2 = 64.f;
+// Smallest |1 - R/Q| the residual variant's single sweep carries as a row
+// factor (its cached columns are stored divided by it).
+constexpr float YREL_MIN_FACTOR = 1.f / 65536.f;
 
 // Per-launch schedule, resolved on the device at kernel start.
 struct Sched {
@@ -370,7 +375,8 @@ __device__ __forceinline__ uint32_t gather_chunk(const GemmParams& p, const uint
 // gather of z/tau at the row's cached indices that fall inside the tile.
 // EXCL (residual-mass variant): the partial leaves out the cached columns, so
 // that the mass outside the cache is a sum of its own terms, never 1 minus
-// the cached mass.
+// the cached mass (the chunk's reference zc still includes them; a chunk with
+// only cached columns adds 0 to the sum).
 // STOREZ (single sweep): the launch covers rows rowmap[rowmap_base + local row]
 // of one chunk, valid rows first; the partial goes to part[tile][local row].
 // Warps holding valid rows also store, for the contractions that follow, each
@@ -429,26 +435,8 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
     uint32_t r[32];
     tmem_ld32(tmem_row + static_cast<uint32_t>(acc * 256 + cc * 32), r);
     tmem_ld_wait(r);
-    if (EXCL) {  // gather first, then sum the columns the gather did not hit
-      const uint32_t hit = gather_chunk(p, r, cb, grow, srow, pos, nxt);
-      float u[32];
-      float cm = -CUDART_INF_F;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        u[j] = (cb + j < p.N && !((hit >> j) & 1u)) ? __uint_as_float(r[j]) * p.c_log2
-                                                     : -CUDART_INF_F;
-        cm = fmaxf(cm, u[j]);
-      }
-      const float mn = fmaxf(m, cm);
-      if (mn != -CUDART_INF_F) {  // else nothing outside the cache so far
-        float cs = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) cs += ex2f(u[j] - mn);
-        s = s * ex2f(m - mn) + cs;
-        m = mn;
-      }
-      continue;
-    }
+    // EXCL: the gather first, so that the sum below can leave out the columns it hit
+    const uint32_t hit = EXCL ? gather_chunk(p, r, cb, grow, srow, pos, nxt) : 0u;
     // The chunk's largest raw logit zc inside the vocabulary (c > 0, so c zc is
     // the largest scaled one), then y_j = 2^(c z_j - c zc) in (0, 1]: one FFMA
     // and one ex2 per element give the lse term and, in the single sweep, the
@@ -475,7 +463,11 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
       const float y1 = (full || cb + 2 * j + 1 < p.N)
                            ? ex2f(fmaf(__uint_as_float(r[2 * j + 1]), p.c_log2, -uzc))
                            : 0.f;
-      cs = __fadd_rn(__fadd_rn(cs, y0), y1);
+      if (EXCL)  // the columns outside the row's cache only
+        cs = __fadd_rn(__fadd_rn(cs, ((hit >> (2 * j)) & 1u) ? 0.f : y0),
+                       ((hit >> (2 * j + 1)) & 1u) ? 0.f : y1);
+      else
+        cs = __fadd_rn(__fadd_rn(cs, y0), y1);
       if (STOREZ) {
         const __nv_bfloat162 hb = __floats2bfloat162_rn(__fmul_rn(y0, f), __fmul_rn(y1, f));
         hy[j] = *reinterpret_cast<const uint32_t*>(&hb);
@@ -505,7 +497,7 @@ __device__ __forceinline__ void epi_fwd(const GemmParams& p, const Sched& sc_, c
         ++piece;
       }
     }
-    gather_chunk(p, r, cb, grow, srow, pos, nxt);
+    if (!EXCL) gather_chunk(p, r, cb, grow, srow, pos, nxt);
   }
   tc_fence_before();
   mbar_arrive(&tempty[acc]);
@@ -924,7 +916,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  // [pipeline stages][epilogue staging (EPI_DW, EPI_DZ, EPI_TMAX, EPI_FWDZ)][barriers, TMEM slot,
+  // [pipeline stages][epilogue staging (EPI_DW, EPI_DZ, EPI_TMAX, EPI_FWDZ*)][barriers, TMEM slot,
   // abort flag]
   float* epi_stage = reinterpret_cast<float*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.stages) * p.stage_bytes +
@@ -984,10 +976,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (MODE == EPI_DW)
         epi_dw(p, sc, c, acc, tmem_row, q, tfull, tempty, use, abort_flag, ok, &tmC, &tmD,
                my_stage, piece);
-      else if (MODE == EPI_FWD || MODE == EPI_FWD_RESID || MODE == EPI_FWDZ)
-        epi_fwd<MODE == EPI_FWD_RESID, MODE == EPI_FWDZ>(p, sc, c, acc, tmem_row, r_in_tile,
-                                                         tfull, tempty, use, abort_flag, ok, &tmC,
-                                                         my_stage, piece);
+      else if (MODE == EPI_FWD || MODE == EPI_FWD_RESID || MODE == EPI_FWDZ ||
+               MODE == EPI_FWDZ_RESID)
+        epi_fwd<MODE == EPI_FWD_RESID || MODE == EPI_FWDZ_RESID,
+                MODE == EPI_FWDZ || MODE == EPI_FWDZ_RESID>(p, sc, c, acc, tmem_row, r_in_tile,
+                                                            tfull, tempty, use, abort_flag, ok,
+                                                            &tmC, my_stage, piece);
       else if (MODE == EPI_DZ)
         epi_dz(p, sc, c, acc, tmem_row, r_in_tile, tfull, tempty, use, abort_flag, ok, &tmC,
                my_stage, piece);
@@ -1001,7 +995,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
     }
     // the TMA copies this warp issued finish before the CTA leaves
-    if ((MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX || MODE == EPI_FWDZ) && lane == 0)
+    if ((MODE == EPI_DW || MODE == EPI_DZ || MODE == EPI_TMAX || MODE == EPI_FWDZ ||
+         MODE == EPI_FWDZ_RESID) && lane == 0)
       bulk_wait_group_all();
   }
   tc_fence_before();
@@ -1131,15 +1126,18 @@ __device__ __forceinline__ float merge_lse(const float (&sm)[COMBINE_SPLIT][32],
 
 // The single sweep's scales of the chunk's stored values, formed with the lse
 // (rscale == null everywhere else).  For local row i below the chunk's valid
-// count: escale[i] = exp(o_i / tau - lse) and rscale[i] = s escale[i], with
-// s = grad_loss / N_valid / tau, so that G = rscale times the stored values;
-// *oscale = s.  When the chunk is flagged (ovf), its G is recomputed whole and
-// the scales are 1.  Rows past the valid count get 0.  valid_only: the logit
-// GEMM covered the chunk's valid rows only, so the other rows get lse = NaN and
-// row_kl = 0 without reading partials.
+// count: escale[i] = exp(o_i / tau - lse) g_i and rscale[i] = s escale[i], with
+// s = grad_loss / N_valid / tau and g_i = 1 - R/Q for the residual-mass variant
+// (1 for the main loss), so that G = rscale times the stored values away from
+// the cached columns; *oscale = s.  Rows past the valid count get 0.  A row
+// with |g| below YREL_MIN_FACTOR (R close to Q) flags the chunk (ovf), whose
+// G is then recomputed whole; the cached-column pass then sets the scales to
+// 1.  valid_only: the logit GEMM covered the chunk's valid rows only, so the
+// other rows get lse = NaN (and Q = NaN) and row_kl = 0 without reading
+// partials.
 struct SweepScales {
   const float* roff;
-  const int* ovf;
+  int* ovf;
   const int* nvalid;
   float grad_loss, inv_tau;
   float* rscale;
@@ -1181,27 +1179,12 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
     const float L = merge_lse(sm, ss, x);
     s_lse[x] = L;
     if (in && lse_out && !resid) lse_out[row] = live ? L : CUDART_NAN_F;
-    if (sw.rscale) {  // uniform
-      const int nv = *sw.nvalid;
-      const bool redo = *sw.ovf != 0;
-      const float sg = nv > 0 ? sw.grad_loss / static_cast<float>(nv) * sw.inv_tau : 0.f;
-      if (in) {
-        float e = 0.f, c = 0.f;
-        if (li < nv - rowmap_base) {
-          e = redo ? 1.f : expf(sw.roff[li] * sw.inv_tau - L);
-          c = redo ? 1.f : sg * e;
-        }
-        sw.escale[li] = e;
-        sw.rscale[li] = c;
-      }
-      if (blockIdx.x == 0 && x == 0) *sw.oscale = redo ? 1.f : sg;
-    }
   }
   __syncthreads();
   if (resid) {  // uniform: the cached columns complete the normaliser
     m = -CUDART_INF_F;
     s = 0.f;
-    if (in)
+    if (live)
       for (int k = y; k < K; k += COMBINE_SPLIT)
         if (k == 0 || sidx[rk0 + k] != sidx[rk0 + k - 1]) online_lse_add(zg[rk0 + k], m, s);
     sm[y][x] = m;
@@ -1213,7 +1196,7 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
       const float L = fmaxf(Lu, Lc) + log1pf(expf(-fabsf(Lu - Lc)));  // Lc is finite
       s_lu[x] = Lu;
       s_lse[x] = L;
-      if (in && lse_out) lse_out[row] = L;
+      if (in && lse_out) lse_out[row] = live ? L : CUDART_NAN_F;
     }
     __syncthreads();
   }
@@ -1243,7 +1226,7 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
         const float lu = s_lu[x] - lse;
         Q = expf(lu) - dup;
         logQ = dup == 0.f ? lu : logf(Q);
-        if (outside_mass_out) outside_mass_out[row] = Q;
+        if (outside_mass_out) outside_mass_out[row] = live ? Q : CUDART_NAN_F;
       }
       float rk = 0.f;
       if (live && valid[row]) {
@@ -1255,8 +1238,29 @@ __global__ void __launch_bounds__(32 * COMBINE_SPLIT)
       }
       if (row_kl_out) row_kl_out[row] = rk;
       kl = rk;
+      if (sw.rscale) {  // uniform: the single sweep's scales of this row's stored values
+        const int nv = *sw.nvalid;
+        float e = 0.f, c = 0.f;
+        if (li < nv - rowmap_base) {  // a valid row of the chunk
+          float g = 1.f;
+          if (resid) {
+            const float R = resid[row];
+            if (R > 0.f) g = 1.f - R / Q;
+          }
+          if (!(fabsf(g) >= YREL_MIN_FACTOR)) *sw.ovf = 1;  // (also a NaN factor)
+          const float sg = sw.grad_loss / static_cast<float>(nv) * sw.inv_tau;
+          e = expf(sw.roff[li] * sw.inv_tau - lse) * g;
+          c = sg * e;
+        }
+        sw.escale[li] = e;
+        sw.rscale[li] = c;
+      }
     }
     red[x] = kl;
+    if (sw.rscale && blockIdx.x == 0 && x == 0) {
+      const int nv = *sw.nvalid;
+      *sw.oscale = nv > 0 ? sw.grad_loss / static_cast<float>(nv) * sw.inv_tau : 0.f;
+    }
   }
   __syncthreads();
   if (y == 0 && x == 0 && losspart) {
@@ -1462,16 +1466,21 @@ __global__ void kd_gather_rows_offset_kernel(const uint4* __restrict__ h,
   if (lane == 0) roff[i] = acc;
 }
 
-// Single sweep, after the combine: completes the chunk's stored values so that
-// G = rscale times them.  At each distinct cached column v of a valid local row
-// i (original row t) the value becomes exp((z_v - o) / tau) - P exp(lse - o/tau),
-// P the teacher probability summed over the slots naming v, from the fp32
-// z_v / tau of the gather (one rounding to bf16, as for G itself).  Rows from
-// the valid count up to the next multiple of 64 (within c_cap) are set to 0:
-// the dW contraction reads whole 64-row steps of the buffer against zero rows
-// of h_c^T, and what an earlier chunk left there must not add NaN.  A chunk
-// flagged by the logit GEMM (ovf) has its G recomputed whole before this
-// kernel, which then only writes the zero rows.  One warp per row, the lanes
+// Single sweep, after the combine and the gated recompute: completes the
+// chunk's stored values so that G = rscale times them.  At each distinct cached
+// column v of a valid local row i (original row t) the value becomes
+//   (exp((z_v - o)/tau) a_v - P exp(lse - o/tau)) / g,
+// P the teacher probability summed over the c_v slots naming v, from the fp32
+// z_v / tau of the gather (one rounding to bf16, as for G itself).  Main loss:
+// a_v = g = 1.  Residual-mass variant (resid != null): rq = R/Q (0 when
+// R = 0), g = 1 - rq, a_v = 1 + (c_v - 1) rq, so that rscale times the value
+// is s (q_v a_v - P) with no cancellation between the two parts of a_v.  Rows
+// from the valid count up to the next multiple of 64 (within c_cap) are set to
+// 0: the dW contraction reads whole 64-row steps of the buffer against zero
+// rows of h_c^T, and what an earlier chunk left there must not add NaN.  A
+// chunk flagged (ovf) by the logit GEMM or the combine has had its G
+// recomputed whole: then this kernel only writes the zero rows and sets the
+// valid rows' scales (and the dW factor) to 1.  One warp per row, the lanes
 // over the row's sorted slots (a repeated index is handled by the first slot
 // of its run, so no two lanes write one column).
 constexpr int FIX_WARPS = 8;
@@ -1482,7 +1491,9 @@ __global__ void __launch_bounds__(32 * FIX_WARPS)
                          const int* __restrict__ sidx, const float* __restrict__ sp,
                          const float* __restrict__ zg, int K, const float* __restrict__ lse,
                          const float* __restrict__ roff, float inv_tau,
-                         const int* __restrict__ ovf) {
+                         const float* __restrict__ resid, const float* __restrict__ outside_mass,
+                         const int* __restrict__ ovf, float* __restrict__ rscale,
+                         float* __restrict__ escale, float* __restrict__ oscale) {
   const int rows = max(0, min(*nvalid - c0, c_cap));
   const int tail_end = min(c_cap, (rows + 63) & ~63);
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -1490,12 +1501,25 @@ __global__ void __launch_bounds__(32 * FIX_WARPS)
   const int64_t n16 = static_cast<int64_t>(tail_end - rows) * (V / 8);  // V % 8 == 0
   uint4* tail = reinterpret_cast<uint4*>(gbuf + static_cast<int64_t>(rows) * V);
   for (int64_t e = tid; e < n16; e += nthreads) tail[e] = make_uint4(0u, 0u, 0u, 0u);
-  if (*ovf) return;
+  if (*ovf) {  // G was recomputed: it needs no scale
+    for (int64_t i = tid; i < rows; i += nthreads) {
+      rscale[i] = 1.f;
+      escale[i] = 1.f;
+    }
+    if (tid == 0) *oscale = 1.f;
+    return;
+  }
   const int lane = threadIdx.x & 31;
   for (int64_t i = tid >> 5; i < rows; i += nthreads >> 5) {
     const int64_t t = rowmap[c0 + i];
     const float oi = roff[i] * inv_tau;
     const float e2 = expf(lse[t] - oi);
+    float rq = 0.f;
+    if (resid) {
+      const float R = resid[t];
+      if (R > 0.f) rq = R / outside_mass[t];
+    }
+    const float g = 1.f - rq;
     const int* srow = sidx + t * K;
     const float* prow = sp + t * K;
     const float* zrow = zg + t * K;
@@ -1504,8 +1528,10 @@ __global__ void __launch_bounds__(32 * FIX_WARPS)
       const int v = srow[k];
       if ((k > 0 && srow[k - 1] == v) || v < 0 || v >= V) continue;
       float P = prow[k];
-      for (int q = k + 1; q < K && srow[q] == v; ++q) P += prow[q];
-      grow[v] = __float2bfloat16_rn(expf(zrow[k] - oi) - P * e2);
+      int cnt = 1;
+      for (int q = k + 1; q < K && srow[q] == v; ++q, ++cnt) P += prow[q];
+      const float a = cnt == 1 ? 1.f : 1.f + static_cast<float>(cnt - 1) * rq;
+      grow[v] = __float2bfloat16_rn((expf(zrow[k] - oi) * a - P * e2) / g);
     }
   }
 }

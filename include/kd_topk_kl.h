@@ -235,6 +235,29 @@ int kd_topk_kl_backward_residual(const void* h, const void* W, const int32_t* te
                                  const float* outside_mass, float grad_loss, float* dh, float* dW,
                                  void* ws, size_t ws_bytes, int32_t* dev_status,
                                  struct CUstream_st* stream);
+/*
+ * The residual-mass variant's training step in one call, as
+ * kd_topk_kl_forward_backward for the main loss: the same single sweep, with
+ * the lse partials over the columns outside the cache, and the per-row factor
+ * of the stored values times g = 1 - R/Q (every uncached column's gradient is
+ * s q (1 - R/Q)); the cached columns are rewritten as s (q (1 + (c - 1) R/Q) - P)
+ * divided by that factor.  A chunk with a row where |1 - R/Q| < 2^-16 (R close
+ * to Q) has its G recomputed from the lse, like a chunk whose stored values
+ * would leave range.  outside_mass (fp32 [T], device) is required and written
+ * as kd_topk_kl_forward_residual writes it.  Results: loss, lse, row_kl and
+ * outside_mass equal kd_topk_kl_forward_residual's bit for bit; dh and dW equal
+ * kd_topk_kl_backward_residual's to within bf16 rounding.  Flags, workspace
+ * (kd_topk_kl_forward_backward_workspace_size) and errors as
+ * kd_topk_kl_forward_backward.
+ */
+int kd_topk_kl_forward_backward_residual(const void* h, const void* W, const int32_t* teacher_idx,
+                                         const float* teacher_logits, const float* teacher_lse,
+                                         const uint8_t* valid, int64_t T, int64_t V, int64_t d,
+                                         int32_t K, float tau, int64_t chunk, float grad_loss,
+                                         uint32_t flags, float* loss, float* lse, float* row_kl,
+                                         float* outside_mass, float* dh, float* dW, void* ws,
+                                         size_t ws_bytes, int32_t* dev_status,
+                                         struct CUstream_st* stream);
 
 /*
  * Teacher-side top-K cache producer (aipuls.nl summary, section "Summary": the

@@ -301,3 +301,21 @@ def test_wrappers_reject_tensors_off_the_current_device(monkeypatch):
             kd.kd_topk_kl_forward(kw["h"], kw["W"], kw["teacher_idx"], kw["teacher_logits"],
                                   kw["valid"], 1.0, 4, kw["loss"], kw["lse"], ws=ws,
                                   dev_status=_FakeCuda((1,), torch.int32, 0))
+
+
+def test_residual_forward_backward_argument_checks():
+    """The residual training step needs teacher_lse and outside_mass, takes the
+    same flags as kd_topk_kl_forward_backward and the same workspace."""
+    vp = ctypes.c_void_p
+    L = kd.lib()
+    T, V, d, K, chunk = 64, 1024, 64, 8, 64
+    sw, _ = kd.kd_topk_kl_forward_backward_workspace_size(T, V, d, K, chunk)
+
+    def call(tlse=A, mass=A, flags=0, ws_bytes=sw):
+        return L.kd_topk_kl_forward_backward_residual(
+            vp(A), vp(A), vp(A), vp(A), vp(tlse), vp(A), T, V, d, K, 1.0, chunk, 1.0, flags,
+            vp(A), vp(A), None, vp(mass), vp(A), vp(A), vp(A), ws_bytes, vp(A), None)
+    assert call(tlse=None) == INVALID
+    assert call(mass=None) == INVALID
+    assert call(flags=4) == INVALID
+    assert call(ws_bytes=sw - 1) == WORKSPACE

@@ -1,7 +1,8 @@
-"""The residual-mass variant (kd_topk_kl_forward_residual / _backward_residual)
-through the C ABI against its fp64 oracle, with the project's tolerances, on
-seeded inputs spanning several tiles with ragged tails; plus the special case
-with no residual mass, which must agree with the main loss."""
+"""The residual-mass variant (kd_topk_kl_forward_residual / _backward_residual,
+and the one-call kd_topk_kl_forward_backward_residual) through the C ABI
+against its fp64 oracle, with the project's tolerances, on seeded inputs
+spanning several tiles with ragged tails; plus the special case with no
+residual mass, which must agree with the main loss."""
 
 import numpy as np
 import pytest
@@ -165,3 +166,97 @@ def test_residual_student_mass_concentrated_on_the_cache():
     dh, dW = RO.backward(*args, 1.0, f["lse"], f["topk_mass"])
     assert rel_l2(gpu["dh"], dh) <= GRAD_RL2
     assert rel_l2(gpu["dW"], dW) <= GRAD_RL2
+
+
+def run_sweep_resid(x, tlse, chunk, grad_loss=1.0, valid_rows_only=False):
+    """The residual variant's one-call training step (the single sweep)."""
+    g = to_device(x)
+    T, d = g["h"].shape
+    V, K = g["W"].shape[0], g["teacher_idx"].shape[1]
+    m = kd.TopKKL(T, V, d, K, chunk, fused=True)
+    m.forward_backward_residual(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"],
+                                tlse.to("cuda").contiguous(), g["valid"], g["tau"], grad_loss,
+                                valid_rows_only=valid_rows_only)
+    torch.cuda.synchronize()
+    out = dict(status=int(m.status.item()), loss=float(m.loss.item()),
+               lse=m.lse.double().cpu().numpy(), row_kl=m.row_kl.double().cpu().numpy(),
+               outside_mass=m.outside_mass.double().cpu().numpy(),
+               dh=m.dh.double().cpu().numpy(), dW=m.dW.double().cpu().numpy())
+    del m
+    return out
+
+
+# sweep against the separate calls: up to three independent bf16 roundings of G
+# and h_c^T (see test_gpu_fused.py)
+SWEEP_RL2 = 5e-3
+
+
+@pytest.mark.parametrize("name,over,chunk", CASES, ids=[c[0] for c in CASES])
+def test_residual_sweep_matches_split_and_oracle(name, over, chunk):
+    """The residual variant's training step in one call: loss, lse, row_kl and
+    the mass outside the cache bit for bit those of the separate calls, dh and
+    dW within bf16 rounding of them, everything held to the oracle."""
+    x = make_inputs(workload("small_4k", **over))
+    tlse = teacher_full_lse(x["teacher_logits"], x["tau"])
+    a = run_gpu_resid(x, tlse, chunk, grad_loss=0.8)
+    b = run_sweep_resid(x, tlse, chunk, grad_loss=0.8)
+    assert b["status"] == 0
+    assert a["loss"] == b["loss"]
+    for k in ("lse", "row_kl", "outside_mass"):
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    for k in ("dh", "dW"):
+        assert rel_l2(b[k], a[k]) <= SWEEP_RL2, k
+    P = oracle_inputs(x)
+    tl64 = tlse.double().numpy()
+    args = (P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tl64, P["valid"], P["tau"])
+    f = RO.forward(*args)
+    dh, dW = RO.backward(*args, 0.8, f["lse"], f["topk_mass"])
+    assert abs(b["loss"] - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert rel_l2(b["dh"], dh) <= GRAD_RL2 and rel_l2(b["dW"], dW) <= GRAD_RL2
+    assert np.all(b["dh"][P["valid"] == 0] == 0.0)
+
+
+@pytest.mark.parametrize("case", ["concentrated", "recomputed"])
+def test_residual_sweep_concentrated_and_recomputed(case):
+    """The residual sweep where the student puts nearly all its mass on its
+    cache (the cache holds the student's own top entries; the stored values
+    carry it), and where the student's logits lie far above its logit at the
+    teacher's top entry (random cache, logits of standard deviation about 400:
+    the stored values would leave their range, so every chunk's G is recomputed
+    from the lse), against the oracle."""
+    rng = np.random.default_rng(31)
+    T, d, V, K, tau = 320, 256, 6144, 48, 1.0
+    wscale = 1.0 if case == "concentrated" else 40.0
+    h = torch.from_numpy(rng.standard_normal((T, d)).astype(np.float32)).to(torch.bfloat16)
+    Ws = rng.standard_normal((V, d)) * (10.0 * wscale / np.sqrt(d))
+    W = torch.from_numpy(Ws.astype(np.float32)).to(torch.bfloat16)
+    z = h.double().numpy() @ W.double().numpy().T
+    order = np.argsort(-z, axis=1, kind="stable")
+    if case == "concentrated":
+        idx = order[:, :K].astype(np.int32)
+    else:  # random entries away from the student's top 64, so that Q stays near 1
+        idx = np.stack([rng.choice(order[t, 64:], K, replace=False) for t in range(T)])
+        idx = idx.astype(np.int32)
+    first = 8.0 + rng.gumbel(0.0, 1.0, size=(T, 1))
+    tl = np.concatenate([first, first - np.cumsum(rng.exponential(0.3, (T, K - 1)), axis=1)],
+                        axis=1).astype(np.float32)
+    valid = np.ones(T, dtype=np.uint8)
+    valid[rng.choice(T, T // 8, replace=False)] = 0
+    x = dict(h=h, W=W, teacher_idx=torch.from_numpy(idx), teacher_logits=torch.from_numpy(tl),
+             valid=torch.from_numpy(valid), tau=tau)
+    tlse = teacher_full_lse(x["teacher_logits"], tau, seed=31)
+    b = run_sweep_resid(x, tlse, 128)
+    assert b["status"] == 0
+    P = oracle_inputs(x)
+    tl64 = tlse.double().numpy()
+    args = (P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tl64, P["valid"], P["tau"])
+    f = RO.forward(*args)
+    assert abs(b["loss"] - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert np.abs(b["lse"] - f["lse"]).max() <= LSE_ATOL
+    Q = 1.0 - f["topk_mass"]
+    if case == "concentrated":
+        assert np.all(np.abs(b["outside_mass"] - Q) <= 1e-3 * Q)
+    dh, dW = RO.backward(*args, 1.0, f["lse"], f["topk_mass"])
+    for k, ref in (("dh", dh), ("dW", dW)):
+        assert np.all(np.isfinite(b[k])), k
+        assert rel_l2(b[k], ref) <= GRAD_RL2, k
