@@ -1,5 +1,6 @@
 """Host-side logic of the benchmark: clock-record parsing, whole-job
-throughput, and the N > 1 path (barrier + max over ranks) on two gloo ranks."""
+throughput, the N > 1 path (barrier + max over ranks) on two gloo ranks, the
+per-kernel rate table and the lookup of committed DRAM-traffic figures."""
 
 import os
 import socket
@@ -63,3 +64,41 @@ def test_two_rank_max_and_throughput():
 def test_single_rank_helpers():
     assert bench.max_over_ranks(3.0, 1) == 3.0
     bench.barrier(1)
+
+
+def test_kernel_table_rates():
+    """Contractions get TFLOP/s from 2 rows d V per launch (the forward over the
+    rows whose logits are formed, the backward over the valid rows); the single
+    sweep's gated recompute gets a time but no rate; the cached-column pass is
+    rated in GB/s from 14 K bytes per valid row."""
+    ks = {"logits_fwd": (4, 40.0), "logits_bwd": (4, 0.1), "dh": (4, 36.0), "dW": (4, 38.0),
+          "sweep_fix": (4, 0.2)}
+    T, nv, d, V, K = 1000, 900, 64, 5000, 10
+    t = bench.kernel_table(ks, 2, T, nv, d, V, K, sweep=True)
+    assert t["logits_fwd"]["flops_per_launch"] == 2.0 * T * d * V * 2 / 4
+    assert t["dh"]["flops_per_launch"] == 2.0 * nv * d * V * 2 / 4
+    assert "tflops" not in t["logits_bwd"] and "note" in t["logits_bwd"]
+    assert t["sweep_fix"]["bytes_per_launch"] == 14.0 * K * nv * 2 / 4
+    split = bench.kernel_table(ks, 2, T, nv, d, V, K, sweep=False)
+    assert split["logits_bwd"]["flops_per_launch"] == 2.0 * nv * d * V * 2 / 4
+
+
+def test_traffic_matches_workload_and_chunk(tmp_path, monkeypatch):
+    """A committed DRAM-traffic figure is reported only for the workload and
+    chunk size it was captured on, and only while the device code hashes the
+    same."""
+    import json
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    h = bench.device_source_sha256()
+    (prof / "traffic.json").write_text(json.dumps({
+        "dh": {"bytes_per_launch": 123, "workload": "ctx_32k", "chunk": 8192, "device_sha256": h},
+        "dW": {"bytes_per_launch": 456, "workload": "ctx_32k", "chunk": 8192,
+               "device_sha256": "0" * 64}}))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "device_source_sha256", lambda: h)
+    assert bench.load_traffic("dh", "ctx_32k", 8192) == 123
+    assert bench.load_traffic("dh", "ctx_32k", 4096) is None
+    assert bench.load_traffic("dh", "ctx_8k", 8192) is None
+    assert bench.load_traffic("dW", "ctx_32k", 8192) is None
+    assert bench.load_traffic("nothing", "ctx_32k", 8192) is None
