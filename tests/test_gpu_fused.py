@@ -229,3 +229,30 @@ def test_valid_rows_only(chunk):
     f = O.forward(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], P["valid"], P["tau"])
     assert abs(float(b.loss.item()) - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
     assert np.abs(b.lse[v].double().cpu().numpy() - f["lse"][P["valid"] != 0]).max() <= LSE_ATOL
+
+
+def test_sweep_duplicate_indices():
+    """Repeated teacher indices in a row: the cached-column pass writes each
+    repeated column once, from the probabilities of all its slots."""
+    x = make_inputs(workload("small_4k", T=200, d=128, V=1024, K=32, tau=1.0, idx_kind="uniform"))
+    idx = x["teacher_idx"].clone()
+    idx[::3, 5] = idx[::3, 0]
+    idx[1::3, 31] = idx[1::3, 30]
+    idx[2::7, 10] = idx[2::7, 11]
+    idx[2::7, 12] = idx[2::7, 11]
+    x["teacher_idx"] = idx
+    g = to_device(x)
+    a = _separate(g, 64, 1.0)
+    b = kd.TopKKL(200, 1024, 128, 32, 64, fused=True)
+    b.forward_backward(g["h"], g["W"], g["teacher_idx"], g["teacher_logits"], g["valid"], g["tau"],
+                       1.0)
+    torch.cuda.synchronize()
+    kd.check_device_status(b.status, "sweep")
+    for k in ("loss", "lse", "row_kl"):
+        assert torch.equal(getattr(a, k), getattr(b, k)), k
+    P = oracle_inputs(x)
+    args = (P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], P["valid"], P["tau"])
+    f = O.forward(*args)
+    dh, dW = O.backward(*args, 1.0, lse=f["lse"])
+    assert rel_l2(b.dh.double().cpu().numpy(), dh) <= GRAD_RL2
+    assert rel_l2(b.dW.double().cpu().numpy(), dW) <= GRAD_RL2

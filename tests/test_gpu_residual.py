@@ -260,3 +260,37 @@ def test_residual_sweep_concentrated_and_recomputed(case):
     for k, ref in (("dh", dh), ("dW", dW)):
         assert np.all(np.isfinite(b[k])), k
         assert rel_l2(b[k], ref) <= GRAD_RL2, k
+
+
+def test_residual_sweep_duplicates_and_valid_rows_only():
+    """The residual one-call step with repeated teacher indices (a column named
+    by c slots carries c (R/Q) q) and packed masking, with and without
+    KD_VALID_ROWS_ONLY: the flag leaves everything bit for bit the same except
+    the masked rows' lse and outside mass (NaN); both against the oracle."""
+    x = make_inputs(workload("small_4k", T=390, d=192, V=2048, K=24, tau=1.3, idx_kind="uniform",
+                             mask_kind="packed", seq_len=130, pad=25))
+    idx = x["teacher_idx"].clone()
+    idx[::4, 3] = idx[::4, 2]
+    idx[1::5, 23] = idx[1::5, 0]
+    x["teacher_idx"] = idx
+    tlse = teacher_full_lse(x["teacher_logits"], x["tau"])
+    a = run_sweep_resid(x, tlse, 100)
+    b = run_sweep_resid(x, tlse, 100, valid_rows_only=True)
+    assert a["status"] == 0 and b["status"] == 0
+    v = x["valid"].numpy() != 0
+    assert a["loss"] == b["loss"]
+    for k in ("lse", "outside_mass"):
+        np.testing.assert_array_equal(a[k][v], b[k][v], err_msg=k)
+        assert np.all(np.isnan(b[k][~v])), k
+    for k in ("row_kl", "dh", "dW"):
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    s = run_gpu_resid(x, tlse, 100)
+    assert s["loss"] == a["loss"]
+    np.testing.assert_array_equal(s["outside_mass"], a["outside_mass"])
+    P = oracle_inputs(x)
+    tl64 = tlse.double().numpy()
+    args = (P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tl64, P["valid"], P["tau"])
+    f = RO.forward(*args)
+    dh, dW = RO.backward(*args, 1.0, f["lse"], f["topk_mass"])
+    assert abs(a["loss"] - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    assert rel_l2(a["dh"], dh) <= GRAD_RL2 and rel_l2(a["dW"], dW) <= GRAD_RL2
