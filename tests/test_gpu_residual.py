@@ -325,3 +325,38 @@ def test_residual_sweep_full_vocab_small_4k_sampled():
     G = RO.grad_logits_rows(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tl64,
                             P["valid"], P["tau"], 1.0, lse_r, mass_r, n_valid, rows)
     assert rel_l2(b["dh"][rows], G @ P["W"]) <= GRAD_RL2
+
+
+def test_residual_sweep_ctx_32k_sampled():
+    """The headline shapes (T=32768, V=201088, d=2880, chunk 8192) for the
+    residual variant: the one-call step against the separate calls (forward
+    outputs bit for bit, gradients within bf16 rounding) and sampled rows of
+    both against the oracle."""
+    w = workload("ctx_32k")
+    x = make_inputs(w)
+    tlse = teacher_full_lse(x["teacher_logits"], x["tau"])
+    b = run_sweep_resid(x, tlse, w.chunk)
+    assert b["status"] == 0
+    a = run_gpu_resid(x, tlse, w.chunk)
+    assert a["fwd_status"] == 0 and a["bwd_status"] == 0
+    assert a["loss"] == b["loss"]
+    for k in ("lse", "row_kl", "outside_mass"):
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    for k in ("dh", "dW"):
+        assert rel_l2(b[k], a[k]) <= SWEEP_RL2, k
+    P = oracle_inputs(x)
+    rng = np.random.default_rng(7)
+    rows = np.sort(rng.choice(w.T, 16, replace=False))
+    tl64 = tlse.double().numpy()
+    f = RO.forward(P["h"][rows], P["W"], P["teacher_idx"][rows], P["teacher_logits"][rows],
+                   tl64[rows], np.ones(len(rows), dtype=np.uint8), P["tau"])
+    assert np.abs(b["lse"][rows] - f["lse"]).max() <= LSE_ATOL
+    assert np.abs(b["outside_mass"][rows] - (1.0 - f["topk_mass"])).max() <= MASS_ATOL
+    kl = np.where(P["valid"][rows] > 0, f["row_kl"], 0.0)
+    assert np.abs(b["row_kl"][rows] - kl).max() <= LSE_ATOL
+    n_valid = int((P["valid"] > 0).sum())
+    lse_r, mass_r = np.zeros(w.T), np.zeros(w.T)
+    lse_r[rows], mass_r[rows] = f["lse"], f["topk_mass"]
+    G = RO.grad_logits_rows(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tl64,
+                            P["valid"], P["tau"], 1.0, lse_r, mass_r, n_valid, rows)
+    assert rel_l2(b["dh"][rows], G @ P["W"]) <= GRAD_RL2
