@@ -360,3 +360,36 @@ def test_residual_sweep_ctx_32k_sampled():
     G = RO.grad_logits_rows(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tl64,
                             P["valid"], P["tau"], 1.0, lse_r, mass_r, n_valid, rows)
     assert rel_l2(b["dh"][rows], G @ P["W"]) <= GRAD_RL2
+
+
+def test_residual_sweep_teacher_and_student_mass_equal():
+    """Rows where the teacher leaves out exactly the student's mass outside the
+    cache (R = Q, so 1 - R/Q vanishes up to rounding and the row factor cannot
+    carry the cached columns): the one-call step recomputes those chunks' G
+    and still matches the separate calls and the oracle."""
+    x = make_inputs(workload("small_4k", T=384, d=128, V=4096, K=32, tau=1.0, idx_kind="uniform"))
+    P = oracle_inputs(x)
+    a64 = P["teacher_logits"] / P["tau"]
+    m = a64.max(axis=1, keepdims=True)
+    lse_k = (m + np.log(np.exp(a64 - m).sum(axis=1, keepdims=True)))[:, 0]
+    tlse = teacher_full_lse(x["teacher_logits"], x["tau"]).double().numpy()
+    f0 = RO.forward(P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tlse, P["valid"],
+                    P["tau"])
+    rows = np.arange(0, 384, 5)
+    tlse[rows] = lse_k[rows] - np.log(f0["topk_mass"][rows])  # R = 1 - sum P = Q
+    tl32 = torch.from_numpy(tlse.astype(np.float32))
+    tl64 = tl32.double().numpy()
+    a = run_gpu_resid(x, tl32, 128)
+    b = run_sweep_resid(x, tl32, 128)
+    assert b["status"] == 0
+    assert a["loss"] == b["loss"]
+    for k in ("lse", "row_kl", "outside_mass"):
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    args = (P["h"], P["W"], P["teacher_idx"], P["teacher_logits"], tl64, P["valid"], P["tau"])
+    f = RO.forward(*args)
+    dh, dW = RO.backward(*args, 1.0, f["lse"], f["topk_mass"])
+    assert abs(b["loss"] - f["loss"]) <= LOSS_RTOL * abs(f["loss"])
+    for k, ref in (("dh", dh), ("dW", dW)):
+        assert np.all(np.isfinite(b[k])), k
+        assert rel_l2(b[k], ref) <= GRAD_RL2, k
+        assert rel_l2(b[k], a[k]) <= SWEEP_RL2, k
